@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark: microseconds per dispatch + combine round on one GB300.
+
+A step is one round on one batch of synthetic input, through the C ABI:
+    llmoe_clean(set 0); llmoe_dispatch(set 0); llmoe_clean(set 1); llmoe_combine(set 1)
+on the DeepSeek-V3-shaped decode workload (R=8 simulated ranks, T=128 tokens
+per rank, H=7168 bf16, E=256 experts, top-8, uniform routing) unless
+--workload says otherwise.  Inputs are resident in HBM; L2 is flushed (a
+512 MB write) before every timed step, outside the step's events.
+
+Printed (rank 0, one JSON line): the mean step time as ``value``; the
+effective HBM bandwidth of the algorithmic bytes; per-kernel times; the
+roofline of the dominant kernel against the measured copy bandwidth; the
+end-to-end time of the same round with host buffers (pinned host -> device
+copies of every input and device -> host read of the outputs inside the
+timed region); the CPU oracle timed on a bounded sample on the host; GPU
+clocks sampled during the timed region.
+
+--impl reference times the CPU oracle alone on the host cores (the
+reference arm; rank 0 only when launched with several ranks).
+--gpus N > 1 (under torchrun): N independent replicas, one per GPU (the data
+path does not shard across GPUs here); value is the slowest rank's step time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per dispatch+combine round and effective HBM GB/s (% of 8 TB/s) at 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="dsv3")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (per launch / per round)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(w, n_valid: int, tokens: int) -> dict:
+    """Bytes the path must move, no re-reads or staging counted.
+
+    dispatch = x read + top-k ids read + N messages written + R*E count words
+    combine  = ids + weights read + N expert rows read + output written + R*E flag words
+    clean    = R*E signal words per set
+    """
+    R, H, E, K = w.R, w.H, w.E, w.K
+    disp = R * tokens * 2 * H + R * tokens * K * 8 + n_valid * (4 + 2 * H) + R * E * 8
+    comb = R * tokens * K * 12 + n_valid * 2 * H + R * tokens * 2 * H + R * E * 8
+    clean = R * E * 8
+    return {"dispatch": disp, "combine": comb, "clean": clean, "round": disp + comb + 2 * clean}
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in ("combine_routing_count_prefix_gb300/csrc/llmoe.cu", "include/llmoe.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when there is none or it was taken on different kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+            return int(parts[2]) if parts[3] == digest else None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+
+    try:
+        p = torch.cuda.get_device_properties(device_index)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[device_index] if vis else str(device_index)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_round(inp, w, tokens: int):
+    """One oracle round on the first `tokens` tokens of every rank."""
+    import oracle
+
+    x = np.ascontiguousarray(inp["x"][:, :tokens])
+    idx = np.ascontiguousarray(inp["topk_idx"][:, :tokens])
+    wt = np.ascontiguousarray(inp["topk_w"][:, :tokens])
+    oracle.clean(w.R, w.E)
+    oracle.dispatch(x, idx, w.E, num_max_tokens=w.T)
+    oracle.clean(w.R, w.E)
+    oracle.combine((inp["y_pool"], inp["y_row_map"]), idx, wt, w.H, w.E, num_max_tokens=w.T)
+
+
+def cores_used() -> int:
+    return 1  # the oracle is single-threaded
+
+
+def cpu_baseline(inp, w, budget_s: float) -> dict:
+    """Full oracle rounds until the budget is spent (at least one)."""
+    import oracle
+
+    oracle.build()
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        oracle_round(inp, w, w.T)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() >= t_end or len(times) >= 200:
+            break
+    us = statistics.mean(times) * 1e6
+    return {"value": round(us, 1), "unit": "us/round", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{len(times)} full {w.name} rounds (clean, dispatch, clean, combine) of the single-threaded "
+                      f"C oracle; host has {len(os.sched_getaffinity(0))} cores available"}
+
+
+def run_reference(args, rank: int):
+    import oracle
+    from combine_routing_count_prefix_gb300.inputs import WORKLOADS, make_inputs
+
+    if rank != 0:
+        return
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=args.seed)
+    # size each step's token sample so the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    probe = max(1, w.T // 16)
+    oracle_round(inp, w, probe)
+    per_token = max((time.perf_counter() - t0) / probe, 1e-7)
+    budget_per_step = 120.0 / max(1, args.steps + args.warmup)
+    tokens = int(min(w.T, max(1, budget_per_step / per_token)))
+    for _ in range(args.warmup):
+        oracle_round(inp, w, tokens)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_round(inp, w, tokens)
+        times.append(time.perf_counter() - t0)
+    us_full = statistics.mean(times) * 1e6 * (w.T / tokens)
+    algo = algorithmic_bytes(w, int((inp["topk_idx"] >= 0).sum()), w.T)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us_full, 2), "unit": "us/round", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(times) * 1e3, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic", "effective_gbs": round(algo["round"] / us_full / 1e3, 3),
+        "config": {"workload": w.name, "shape": w.describe(), "seed": args.seed,
+                   "sample": f"each step runs the oracle on {tokens} of {w.T} tokens per rank; value scales the "
+                             f"step time to a full round"},
+        "cpu_baseline": {"value": round(us_full, 2), "unit": "us/round", "cores": cores_used(), "kind": "oracle",
+                         "sample": f"{tokens}/{w.T} tokens per rank per step, {args.steps} steps"},
+        "e2e": {"value": round(us_full, 2), "unit": "us/round", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+
+    from combine_routing_count_prefix_gb300 import build as cuda_build
+
+    cuda_build.build()
+    from combine_routing_count_prefix_gb300 import llmoe
+    from combine_routing_count_prefix_gb300.inputs import WORKLOADS, dense_y, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=args.seed)
+    tokens = w.T
+    n_valid = int((inp["topk_idx"] >= 0).sum())
+    algo = algorithmic_bytes(w, n_valid, tokens)
+
+    dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+    x, idx, wt = dev(inp["x"]), dev(inp["topk_idx"]), dev(inp["topk_w"])
+    y = dev(inp["y_pool"]).index_select(0, dev(inp["y_row_map"])).contiguous()
+    out = torch.empty((w.R, tokens, w.H), dtype=torch.int16, device="cuda")
+    rb = llmoe.RankBuffers(w.T, w.H, w.R, w.E, fill=0)
+    bs0, bs1 = rb.buf_set(0, w.K), rb.buf_set(1, w.K)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        llmoe.llmoe_clean(bs0, stream)
+        llmoe.llmoe_dispatch(x, idx, bs0, stream)
+        llmoe.llmoe_clean(bs1, stream)
+        llmoe.llmoe_combine(y, idx, wt, out, bs1, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    with ClockSampler(gpu_id_for(local_rank)) as clocks:
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            e = ev[i]
+            e[0].record(stream)
+            llmoe.llmoe_clean(bs0, stream)
+            e[1].record(stream)
+            llmoe.llmoe_dispatch(x, idx, bs0, stream)
+            e[2].record(stream)
+            llmoe.llmoe_clean(bs1, stream)
+            e[3].record(stream)
+            llmoe.llmoe_combine(y, idx, wt, out, bs1, stream)
+            e[4].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - wall0
+    step_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    disp_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    comb_ms = [e[3].elapsed_time(e[4]) for e in ev]
+    clean_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in ev]
+    timed = torch.tensor([sum(step_ms), wall], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(timed, op=dist.ReduceOp.MAX)
+    round_us = float(timed[0]) / args.steps * 1e3
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream)
+        if world > 1:
+            t = torch.tensor([e2e["value"]], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["value"] = float(t[0])
+
+    if rank == 0:
+        peak, peak_kind = measured_hbm_peak()
+        d_us = statistics.mean(disp_ms) * 1e3
+        c_us = statistics.mean(comb_ms) * 1e3
+        dom, dom_us = ("dispatch", d_us) if d_us >= c_us else ("combine", c_us)
+        dom_gbs = algo[dom] / dom_us / 1e3
+        traffic = ncu_traffic(dom + "_kernel", w.name)
+        gbs = algo["round"] * world / round_us / 1e3
+        line = {
+            "metric": METRIC, "value": round(round_us, 3), "unit": "us/round", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(round_us / 1e3, 6),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.describe(), "seed": args.seed, "tokens_per_rank": tokens,
+                       "unmasked_entries": n_valid, "parallelism": f"replicas{world}",
+                       "l2": f"flushed before every timed step ({FLUSH_BYTES >> 20} MB write, outside the events)"},
+            "effective_gbs": round(gbs, 1), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "frac_of_measured_hbm": round(gbs / peak, 4),
+            "algorithmic_bytes_per_round": algo["round"],
+            "dispatch_us": round(d_us, 3), "combine_us": round(c_us, 3),
+            "clean_us": round(statistics.mean(clean_ms) * 1e3 / 2, 3),
+            "step_us_median": round(statistics.median(step_ms) * 1e3, 3),
+            "wall_s": round(float(timed[1]), 3),
+            "roofline": {"kernel": dom + "_kernel", "bound": "hbm", "achieved": round(dom_gbs, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                         "traffic": traffic, "algorithmic_bytes": algo[dom]},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clocks.summary(),
+        }
+        if e2e is not None:
+            line["e2e"] = e2e
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(inp, w, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
+    """The same round with every input copied from pinned host memory and the
+    outputs (combine output, both sets' signal words) read back, per step."""
+    import torch
+
+    pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+    hx, hidx, hw = pin(inp["x"]), pin(inp["topk_idx"]), pin(inp["topk_w"])
+    hy = pin(dense_y(inp))
+    hout = torch.empty((w.R, tokens, w.H), dtype=torch.int16).pin_memory()
+    hsig = torch.empty((2, w.R, w.E), dtype=torch.int64).pin_memory()
+    dx, didx, dw = torch.empty_like(hx, device="cuda"), torch.empty_like(hidx, device="cuda"), torch.empty_like(
+        hw, device="cuda")
+    dy = torch.empty_like(hy, device="cuda")
+    dout = torch.empty_like(hout, device="cuda")
+    bs0, bs1 = rb.buf_set(0, w.K), rb.buf_set(1, w.K)
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hidx, hw, hy))
+    d2h = hout.numel() * hout.element_size() + hsig.numel() * hsig.element_size()
+
+    def step():
+        for d, h in ((dx, hx), (didx, hidx), (dw, hw), (dy, hy)):
+            d.copy_(h, non_blocking=True)
+        llmoe.llmoe_clean(bs0, stream)
+        llmoe.llmoe_dispatch(dx, didx, bs0, stream)
+        llmoe.llmoe_clean(bs1, stream)
+        llmoe.llmoe_combine(dy, didx, dw, dout, bs1, stream)
+        hout.copy_(dout, non_blocking=True)
+        hsig[0].copy_(rb.signal_words(0), non_blocking=True)
+        hsig[1].copy_(rb.signal_words(1), non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, args.e2e_steps)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+    return {"value": round(us, 2), "unit": "us/round", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "note": "inputs x, topk_idx, topk_w and the dense expert outputs y copied host->device "
+                                "every step; output and signal words copied back"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

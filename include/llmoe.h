@@ -1,0 +1,185 @@
+/*
+ * llmoe.h -- C ABI of the GB300 (sm_103a) low-latency MoE dispatch / combine
+ * library (libllmoe.so).
+ *
+ * One GPU holds R simulated expert-parallel ranks as R disjoint segments of
+ * one device allocation ("rank buffers").  Each rank buffer has the layout of
+ * LLMoEBufferLayout<bf16> from LL_MoE_Buffers.hpp (rocshmem LL_MoE example):
+ * two buffer sets, each with a send region, a receive region and num_experts
+ * int64 signal words; the combine roles alias the dispatch roles of the same
+ * set.  Messages are one int32 header (the source token index) followed by
+ * `hidden` bf16 values, 4 + 2 * hidden bytes, packed without padding.
+ *
+ * Conventions for every call:
+ *   - All pointers passed to the data-path calls are DEVICE pointers into
+ *     memory the caller allocated; the library never allocates, frees or
+ *     synchronises (except llmoe_get_error, which reads a word back).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and runs asynchronously; buffers must stay alive until it ends.
+ *   - A call returns LLMOE_SUCCESS once its kernel is enqueued.  Argument
+ *     checks are done on the host before any launch: a call that returns
+ *     LLMOE_ERR_INVALID_ARGUMENT or LLMOE_ERR_INVALID_USAGE launched nothing.
+ *     LLMOE_ERR_CUDA reports a launch error (cudaGetLastError).
+ *   - bf16 values travel as their uint16_t bit patterns.
+ *
+ * Sequencing: a set's signal words must be zero before a dispatch or combine
+ * writes them (llmoe_clean zeroes them).  A round alternates sets:
+ *   llmoe_clean(set 0); llmoe_dispatch(set 0); llmoe_clean(set 1);
+ *   llmoe_combine(set 1)
+ * so a combine never overwrites counts that consumers of the dispatch read.
+ */
+#ifndef LLMOE_H_
+#define LLMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols keep default visibility when the library is built with
+ * -fvisibility=hidden. */
+#if defined(__GNUC__)
+#define LLMOE_API __attribute__((visibility("default")))
+#else
+#define LLMOE_API
+#endif
+
+/* A cudaStream_t without including the CUDA headers. */
+struct CUstream_st;
+typedef struct CUstream_st* llmoe_stream_t;
+
+/* Status codes.  The values follow mscclpp.h's mscclppResult_t (Success 0,
+ * UnhandledCudaError 1, InvalidArgument 4, InvalidUsage 5). */
+typedef enum {
+  LLMOE_SUCCESS = 0,
+  LLMOE_ERR_CUDA = 1,
+  LLMOE_ERR_INVALID_ARGUMENT = 4,
+  LLMOE_ERR_INVALID_USAGE = 5
+} llmoe_status_t;
+
+/* Device error-word codes, written only when llmoe_buf_set_t.err is non-NULL
+ * (validate mode); the first error a launch meets wins.  Like the refusal
+ * words of memra-engine tp_ar.rs (barrier_errors), the word is read back
+ * with llmoe_get_error, which drains the stream, so it belongs in tests and
+ * gates, not in the hot loop. */
+#define LLMOE_DEV_OK 0
+#define LLMOE_DEV_BAD_EXPERT 1   /* a top-k id outside [-1, num_experts) */
+#define LLMOE_DEV_DUPLICATE 2    /* one expert twice in one token's top-k */
+#define LLMOE_DEV_STALE_SIGNAL 3 /* a signal word was non-zero on entry (a clean was skipped) */
+#define LLMOE_DEV_SLOT_RANGE 4   /* a bucket overflowed num_max_tokens (only reachable with duplicates) */
+
+/* Library limits (checked on the host). */
+#define LLMOE_MAX_TOPK 32
+#define LLMOE_MAX_EXPERTS 8192
+
+/* One buffer set of the R rank buffers, plus the geometry of one call.
+ *   base           device pointer, 16-byte aligned; rank r's buffer starts at
+ *                  base + r * rank_stride.
+ *   rank_stride    bytes between rank buffers; a multiple of 16 and at least
+ *                  llmoe_layout_bytes(num_max_tokens, hidden, num_ranks,
+ *                  num_experts).
+ *   num_max_tokens T: tokens per rank the layout was sized for (the worst-case
+ *                  micro-batch; "num_max_dispatch_tokens_per_rank").
+ *   num_tokens     tokens per rank in this call, 0 <= num_tokens <= T.
+ *   hidden         H, values per token; a multiple of 8 (16-byte rows).
+ *   num_ranks      R >= 1.
+ *   num_experts    E, a multiple of R, <= LLMOE_MAX_EXPERTS.  Expert e is
+ *                  owned by rank e / (E/R) as local expert e % (E/R).
+ *   num_topk       K, 1 <= K <= min(E, LLMOE_MAX_TOPK).
+ *   set            0 or 1: which of the layout's two buffer sets.
+ *   err            optional device int32 word; NULL turns validation off.
+ *                  With validation off, invalid ids are still skipped and no
+ *                  access leaves the buffers, but nothing is reported. */
+typedef struct {
+  void* base;
+  uint64_t rank_stride;
+  int32_t num_max_tokens;
+  int32_t num_tokens;
+  int32_t hidden;
+  int32_t num_ranks;
+  int32_t num_experts;
+  int32_t num_topk;
+  int32_t set;
+  int32_t* err;
+} llmoe_buf_set_t;
+
+/* Bytes of ONE rank buffer: get_rdma_size_hint<bf16>(num_max_tokens, hidden,
+ * num_ranks, num_experts) of LL_MoE_Buffers.hpp, i.e. LLMoEBufferLayout's
+ * total_bytes = 2 * max(send) + 2 * max(recv) + 2 * 8 * num_experts.
+ * num_ranks does not change the size (it is [[maybe_unused]] there).
+ * Returns 0 when a dimension is < 1, when the layout's "bytes %
+ * sizeof(int) == 0" assertion would fail, or when a size overflows 64 bits.
+ * Host only; touches no device. */
+LLMOE_API size_t llmoe_layout_bytes(int num_max_tokens, int hidden, int num_ranks, int num_experts);
+
+/* Byte offsets, from the start of a rank buffer, of buffer set `set`'s send
+ * region, receive region and signal words (LLMoEBufferLayout, "Assign
+ * pointers"; the combine send / recv / flag of a set are the same addresses
+ * as its dispatch send / recv / count).  Any output pointer may be NULL.
+ * Returns LLMOE_SUCCESS, or LLMOE_ERR_INVALID_ARGUMENT when
+ * llmoe_layout_bytes would return 0 or set is not 0 or 1. */
+LLMOE_API int llmoe_layout_offsets(int num_max_tokens, int hidden, int num_ranks, int num_experts, int set,
+                         uint64_t* send_offset, uint64_t* recv_offset, uint64_t* signal_offset);
+
+/* Routing count / prefix scan, on its own (dispatch and combine run the same
+ * scan inside their kernels and do not need this call).
+ *   topk_idx  device int64 [R][num_tokens][K], -1 = masked.
+ *   slot      device int32 [R][num_tokens][K] out: for an unmasked entry
+ *             (src, t, k) choosing expert e, the number of earlier tokens
+ *             t' < t of src that chose e (ascending source-token order inside
+ *             each (expert, source) bucket); -1 where masked or invalid.
+ *   counts    device int64 [E][R] out: tokens of src that chose e.
+ * Only the geometry fields of `bs` are used (base / rank_stride / set are not
+ * read and may be zero); err as for the other calls. */
+LLMOE_API int llmoe_route(const int64_t* topk_idx, int32_t* slot, int64_t* counts, const llmoe_buf_set_t* bs,
+                llmoe_stream_t stream);
+
+/* Dispatch (LLMoEBuffer dispatch receive buffer and recv-count words).
+ *   x         device bf16 [R][num_tokens][H], rows 16-byte aligned.
+ *   topk_idx  device int64 [R][num_tokens][K], -1 = masked.
+ * For every unmasked entry (src, t, k) choosing expert e, owned by rank
+ * dst = e / L as local expert le = e % L, writes the message
+ * [int32 t][x[src][t][0..H)] at row (le * R + src) * T + slot of rank dst's
+ * set-`set` receive region (recv[le][src][slot]), slot as in llmoe_route.
+ * Then writes rank dst's signal word le * R + src = that bucket's count, for
+ * all R * E words.  Nothing else is written: unused receive rows keep their
+ * contents. */
+LLMOE_API int llmoe_dispatch(const uint16_t* x, const int64_t* topk_idx, const llmoe_buf_set_t* bs,
+                   llmoe_stream_t stream);
+
+/* Combine (LLMoEBuffer combine roles; the expert outputs are gathered in
+ * place instead of being staged through the combine send / recv regions).
+ *   y         device bf16 [E * R * T][H], rows 16-byte aligned: the expert
+ *             outputs in receive-row order, row e * R * T + src * T + slot
+ *             for the entry that occupied recv[le][src][slot] of rank e / L.
+ *   topk_idx  device int64 [R][num_tokens][K], -1 = masked.
+ *   topk_w    device fp32 [R][num_tokens][K].
+ *   out       device bf16 [R][num_tokens][H] out, rows 16-byte aligned;
+ *             must not overlap y.
+ * out[src][t][:] = bf16_rne(sum over ascending k of unmasked entries of
+ * fl32(w * fp32(y_row))), starting from +0.0, each product rounded to fp32
+ * before it is added (no fused multiply-add).  Then writes rank src's
+ * set-`set` signal word e = number of rows expert e returned to src. */
+LLMOE_API int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
+                  const llmoe_buf_set_t* bs, llmoe_stream_t stream);
+
+/* Clean (LLMoEBuffer::clean_meta): zero the num_experts int64 signal words
+ * of buffer set `set` in each of the R rank buffers.  This resets both the
+ * dispatch recv counts and the combine recv flags, which share the words. */
+LLMOE_API int llmoe_clean(const llmoe_buf_set_t* bs, llmoe_stream_t stream);
+
+/* Validate-mode read-back: waits for `stream`, copies *bs->err into *code
+ * (LLMOE_DEV_*) and, if `reset` is non-zero, zeroes the word.  Returns
+ * LLMOE_ERR_INVALID_USAGE when bs->err is NULL. */
+LLMOE_API int llmoe_get_error(const llmoe_buf_set_t* bs, llmoe_stream_t stream, int32_t* code, int reset);
+
+/* A static string for a status code. */
+LLMOE_API const char* llmoe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLMOE_H_ */

@@ -1,0 +1,365 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every test feeds the same seeded inputs to both.  Bars:
+- dispatch: every written message (header + payload) and every recv-count
+  word bit-exact; every other byte of the rank buffers untouched (canary);
+- combine: every output element within 1 bf16 ulp (ordinal distance of the
+  bit patterns <= 1) of the oracle, and in fact bit-exact since both sides
+  round the same products and sums in the same order; flag words exact;
+- route: slots and counts exact.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_routing_count_prefix_gb300.inputs import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+CANARY = 0xA5
+CANARY_WORD = int(np.array([0xA5A5A5A5A5A5A5A5], dtype=np.uint64).view(np.int64)[0])
+OUT_CANARY = 0x7FC1  # a NaN pattern: an unwritten output element fails
+
+
+@pytest.fixture(scope="module")
+def L():
+    from combine_routing_count_prefix_gb300 import build
+
+    build.build()
+    from combine_routing_count_prefix_gb300 import llmoe
+
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    oracle.build()
+    return llmoe
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def y_dev(inp) -> torch.Tensor:
+    pool = dev(inp["y_pool"])
+    return pool.index_select(0, dev(inp["y_row_map"])).contiguous()
+
+
+def ordinal(b: np.ndarray) -> np.ndarray:
+    b = b.astype(np.int32)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def all_equal_chunked(t: torch.Tensor, value: int, chunk=1 << 31) -> bool:
+    flat = t.view(-1)
+    for s in range(0, flat.numel(), chunk):
+        if not bool((flat[s:s + chunk] == value).all()):
+            return False
+    return True
+
+
+class Round:
+    """One clean / dispatch / clean / combine round on fresh canary-filled buffers."""
+
+    def __init__(self, L, w: Workload, seed=0, tokens=None, dispatch_set=0, inp=None, validate=True):
+        self.L, self.w = L, w
+        self.inp = inp if inp is not None else make_inputs(w, seed=seed, tokens=tokens)
+        self.T_call = self.inp["x"].shape[1]
+        self.rb = L.RankBuffers(w.T, w.H, w.R, w.E, guard=256, fill=CANARY)
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda") if validate else None
+        self.ds, self.cs = dispatch_set, 1 - dispatch_set
+        self.bs_d = self.rb.buf_set(self.ds, w.K, self.T_call, self.err)
+        self.bs_c = self.rb.buf_set(self.cs, w.K, self.T_call, self.err)
+        self.x, self.idx, self.wt = dev(self.inp["x"]), dev(self.inp["topk_idx"]), dev(self.inp["topk_w"])
+        self.y = y_dev(self.inp)
+        self.out = torch.full((w.R, self.T_call, w.H), OUT_CANARY, dtype=torch.int16, device="cuda")
+
+    def run(self):
+        L = self.L
+        L.llmoe_clean(self.bs_d)
+        L.llmoe_dispatch(self.x, self.idx, self.bs_d)
+        L.llmoe_clean(self.bs_c)
+        L.llmoe_combine(self.y, self.idx, self.wt, self.out, self.bs_c)
+        torch.cuda.synchronize()
+        return self
+
+    def error(self):
+        return self.L.llmoe_get_error(self.bs_d) if self.err is not None else 0
+
+    def check_dispatch(self, d=None):
+        w, inp = self.w, self.inp
+        if d is None:
+            d = oracle.dispatch(inp["x"], inp["topk_idx"], w.E, num_max_tokens=w.T)
+        recv = self.rb.recv_rows(self.ds)
+        rr, ri = dev(d["row_rank"]), dev(d["row_index"])
+        got = recv[rr, ri].cpu().numpy() if d["n"] else np.zeros((0, 4 + 2 * w.H), np.uint8)
+        assert got.shape == d["msgs"].shape
+        bad = np.nonzero((got != d["msgs"]).any(axis=1))[0]
+        assert bad.size == 0, f"{bad.size} of {d['n']} messages differ; first at entry {bad[:5]}"
+        assert np.array_equal(self.rb.signal_words(self.ds).cpu().numpy(), d["count_words"])
+        return d
+
+    def check_combine(self):
+        w, inp = self.w, self.inp
+        ref, flags = oracle.combine((inp["y_pool"], inp["y_row_map"]), inp["topk_idx"], inp["topk_w"], w.H, w.E,
+                                    num_max_tokens=w.T)
+        got = self.out.cpu().numpy().view(np.uint16)
+        dist = np.abs(ordinal(got) - ordinal(ref))
+        assert dist.max(initial=0) <= 1, f"max ulp distance {dist.max()}"
+        assert int((dist != 0).sum()) == 0, f"{int((dist != 0).sum())} elements differ by 1 ulp"
+        assert np.array_equal(self.rb.signal_words(self.cs).cpu().numpy(), flags)
+
+    def check_canary(self, d):
+        """Nothing outside the written messages and signal words changed."""
+        recv = self.rb.recv_rows(self.ds)
+        if d["n"]:
+            recv[dev(d["row_rank"]), dev(d["row_index"])] = CANARY
+        self.rb.signal_words(0).fill_(CANARY_WORD)
+        self.rb.signal_words(1).fill_(CANARY_WORD)
+        assert all_equal_chunked(self.rb.storage, CANARY)
+
+
+def full_check(r: Round):
+    r.run()
+    assert r.error() == 0
+    d = r.check_dispatch()
+    r.check_combine()
+    r.check_canary(d)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "many_small"])
+def test_workload_full_size(L, name):
+    full_check(Round(L, WORKLOADS[name], seed=0))
+
+
+def test_workload_large(L):
+    w = WORKLOADS["large"]
+    need = L.round_up(L.llmoe_layout_bytes(w.T, w.H, w.R, w.E) + 256, 256) * w.R + w.E * w.R * w.T * w.H * 2
+    free, _ = torch.cuda.mem_get_info()
+    assert free > need + (8 << 30), f"large workload needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free"
+    full_check(Round(L, w, seed=0))
+
+
+# ---------------------------------------------------------------------------
+# shape sweep: odd hidden sizes (every row phase, partial warp chunks), one
+# rank, many ranks, top-1 .. top-8, masks, fewer tokens than the layout
+# ---------------------------------------------------------------------------
+
+SWEEP = []
+for R, Lx in [(1, 8), (2, 4), (32, 1), (3, 5)]:
+    for K in (1, 2, 8):
+        if K > R * Lx:
+            continue
+        for H in (8, 56, 264):
+            for T in (1, 3, 37):
+                SWEEP.append((R, R * Lx, K, H, T))
+
+
+@pytest.mark.parametrize("R,E,K,H,T", SWEEP)
+def test_shape_sweep(L, R, E, K, H, T):
+    w = Workload("sweep", R, T, H, E, K, mask_p=0.3 if K > 1 else 0.0)
+    full_check(Round(L, w, seed=R * 1000 + E * 10 + K + H + T))
+
+
+@pytest.mark.parametrize("tokens", [0, 1, 5, 127])
+def test_fewer_tokens_than_layout(L, tokens):
+    w = WORKLOADS["dsv3"].with_(H=512)
+    full_check(Round(L, w, seed=tokens, tokens=tokens))
+
+
+def test_repeat_after_smaller_call_on_same_buffers(L):
+    w = WORKLOADS["skewed"]
+    r = Round(L, w, seed=1).run()
+    assert r.error() == 0
+    r.check_dispatch()
+    r.check_combine()
+    small = make_inputs(w, seed=2, tokens=9)
+    r2 = Round.__new__(Round)
+    r2.__dict__.update(r.__dict__)
+    r2.inp, r2.T_call = small, 9
+    r2.bs_d = r.rb.buf_set(0, w.K, 9, r.err)
+    r2.bs_c = r.rb.buf_set(1, w.K, 9, r.err)
+    r2.x, r2.idx, r2.wt = dev(small["x"]), dev(small["topk_idx"]), dev(small["topk_w"])
+    r2.y = y_dev(small)
+    r2.out = torch.full((w.R, 9, w.H), OUT_CANARY, dtype=torch.int16, device="cuda")
+    r2.run()
+    assert r2.error() == 0
+    r2.check_dispatch()
+    r2.check_combine()
+
+
+def test_all_tokens_masked(L):
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, seed=0)
+    inp["topk_idx"][:] = -1
+    r = Round(L, w, inp=inp)
+    full_check(r)
+    assert not (r.out != 0).any()
+
+
+def test_maximum_topk_and_experts(L):
+    w = Workload("max", 8, 4, 8, 8192, 32, mask_p=0.05)
+    full_check(Round(L, w, seed=5))
+
+
+def test_long_prefix_many_tokens_per_cta(L):
+    # enough tokens that each CTA takes the maximum token block
+    w = Workload("long", 8, 4864, 8, 16, 3, routing="zipf", zipf_s=1.2, mask_p=0.1)
+    full_check(Round(L, w, seed=6))
+
+
+def test_hot_expert_single_bucket(L):
+    # every token of every rank picks expert 0: one bucket per source holds T rows
+    w = WORKLOADS["skewed"].with_(H=256)
+    inp = make_inputs(w, seed=3)
+    inp["topk_idx"][:, :, 0] = 0
+    inp["topk_idx"][:, :, 1:] = np.where(inp["topk_idx"][:, :, 1:] == 0, -1, inp["topk_idx"][:, :, 1:])
+    full_check(Round(L, w, inp=inp))
+
+
+@pytest.mark.parametrize("name", ["tiny", "many_small"])
+def test_dispatch_into_set_one(L, name):
+    full_check(Round(L, WORKLOADS[name], seed=4, dispatch_set=1))
+
+
+def test_validation_off_gives_same_results(L):
+    full_check(Round(L, WORKLOADS["skewed"].with_(H=1024), seed=8, validate=False))
+
+
+# ---------------------------------------------------------------------------
+# route scan on its own
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "many_small", "large"])
+def test_route_scan(L, name):
+    w = WORKLOADS[name].with_(H=8)
+    inp = make_inputs(w, seed=11)
+    slot_ref, cnt_ref = oracle.route(inp["topk_idx"], w.E)
+    idx = dev(inp["topk_idx"])
+    slot = torch.full(idx.shape, -7, dtype=torch.int32, device="cuda")
+    counts = torch.full((w.E, w.R), -7, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bs = L.llmoe_buf_set_t(base=None, rank_stride=0, num_max_tokens=w.T, num_tokens=w.T, hidden=w.H,
+                           num_ranks=w.R, num_experts=w.E, num_topk=w.K, set=0, err=err.data_ptr())
+    L.llmoe_route(idx, slot, counts, bs)
+    assert L.llmoe_get_error(bs) == 0
+    assert np.array_equal(slot.cpu().numpy(), slot_ref)
+    assert np.array_equal(counts.cpu().numpy(), cnt_ref)
+
+
+# ---------------------------------------------------------------------------
+# the two buffer sets are independent; a round replays in a CUDA graph
+# ---------------------------------------------------------------------------
+
+def test_combine_leaves_dispatch_set_alone(L):
+    w = WORKLOADS["many_small"]
+    r = Round(L, w, seed=9)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch(r.x, r.idx, r.bs_d)
+    torch.cuda.synchronize()
+    snap = r.rb.storage.clone()
+    L.llmoe_clean(r.bs_c)
+    L.llmoe_combine(r.y, r.idx, r.wt, r.out, r.bs_c)
+    torch.cuda.synchronize()
+    r.rb.signal_words(1).copy_(snap.view(torch.int64).as_strided(r.rb.signal_words(1).shape,
+                                                                  r.rb.signal_words(1).stride(),
+                                                                  r.rb.signal_words(1).storage_offset()))
+    assert torch.equal(snap, r.rb.storage)
+
+
+def test_round_in_cuda_graph(L):
+    w = WORKLOADS["skewed"]
+    r = Round(L, w, seed=10)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        r.run()  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        L.llmoe_clean(r.bs_d)
+        L.llmoe_dispatch(r.x, r.idx, r.bs_d)
+        L.llmoe_clean(r.bs_c)
+        L.llmoe_combine(r.y, r.idx, r.wt, r.out, r.bs_c)
+    r.rb.storage.fill_(CANARY)
+    r.out.fill_(OUT_CANARY)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    d = r.check_dispatch()
+    r.check_combine()
+    r.check_canary(d)
+
+
+# ---------------------------------------------------------------------------
+# validate mode: bad input is reported, skipped, and stays in bounds
+# ---------------------------------------------------------------------------
+
+def test_stale_signal_reported(L):
+    w = WORKLOADS["tiny"]
+    r = Round(L, w, seed=0)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch(r.x, r.idx, r.bs_d)
+    assert L.llmoe_get_error(r.bs_d) == L.LLMOE_DEV_OK
+    L.llmoe_dispatch(r.x, r.idx, r.bs_d)  # no clean in between
+    assert L.llmoe_get_error(r.bs_d, reset=True) == L.LLMOE_DEV_STALE_SIGNAL
+    assert L.llmoe_get_error(r.bs_d) == L.LLMOE_DEV_OK
+    L.llmoe_clean(r.bs_c)
+    L.llmoe_combine(r.y, r.idx, r.wt, r.out, r.bs_c)
+    L.llmoe_combine(r.y, r.idx, r.wt, r.out, r.bs_c)
+    assert L.llmoe_get_error(r.bs_c, reset=True) == L.LLMOE_DEV_STALE_SIGNAL
+
+
+@pytest.mark.parametrize("bad", [8, 9, 1 << 40, -2, -(1 << 40)])
+def test_out_of_range_expert_reported_and_skipped(L, bad):
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, seed=1)
+    inp["topk_idx"][1, 3, 1] = bad
+    r = Round(L, w, inp=inp).run()
+    assert r.error() == L.LLMOE_DEV_BAD_EXPERT
+    masked = inp["topk_idx"].copy()
+    masked[1, 3, 1] = -1
+    d = oracle.dispatch(inp["x"], masked, w.E, num_max_tokens=w.T)
+    r.check_dispatch(d)
+    r.check_canary(d)
+
+
+def test_duplicate_expert_reported_in_bounds(L):
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, seed=2)
+    inp["topk_idx"][0, :, 1] = inp["topk_idx"][0, :, 0]  # every token of rank 0 repeats its expert
+    r = Round(L, w, inp=inp).run()
+    assert r.error() in (L.LLMOE_DEV_DUPLICATE, L.LLMOE_DEV_SLOT_RANGE)
+    # only receive rows and signal words may have changed
+    for s in (0, 1):
+        r.rb.recv_rows(s).fill_(CANARY)
+        r.rb.signal_words(s).fill_(CANARY_WORD)
+    assert all_equal_chunked(r.rb.storage, CANARY)
+
+
+def test_error_word_reset(L):
+    err = torch.full((1,), 3, dtype=torch.int32, device="cuda")
+    bs = L.llmoe_buf_set_t(base=None, rank_stride=0, num_max_tokens=1, num_tokens=1, hidden=8, num_ranks=1,
+                           num_experts=1, num_topk=1, set=0, err=err.data_ptr())
+    assert L.llmoe_get_error(bs, reset=True) == 3
+    assert int(err.item()) == 0
+
+
+def test_invalid_call_launches_nothing(L):
+    w = WORKLOADS["tiny"]
+    r = Round(L, w, seed=0)
+    bad = r.rb.buf_set(0, w.K, w.T, r.err)
+    bad.hidden = 12
+    with pytest.raises(L.LLMoEError) as ei:
+        L.llmoe_dispatch(r.x, r.idx, bad)
+    assert ei.value.status == L.LLMOE_ERR_INVALID_ARGUMENT
+    torch.cuda.synchronize()
+    assert all_equal_chunked(r.rb.storage, CANARY)
