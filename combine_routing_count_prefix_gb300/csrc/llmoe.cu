@@ -7,8 +7,8 @@
 // every row read once.
 //
 // Kernels:
-//   route_scan (device function, run at the start of the route, dispatch and
-//     combine kernels): per-(expert, source rank) counts and slots, where the
+//   route scan (route_hist / route_slot, run at the start of the route,
+//     dispatch and combine kernels): per-(expert, source rank) counts and slots, where the
 //     slot of token t for expert e is the number of earlier tokens of the same
 //     source rank that chose e.  Built from a shared-memory histogram of the
 //     tokens before the CTA's block (integer atomics, so the result does not
@@ -36,9 +36,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxTokensPerBlock = 32;
-constexpr int kKBatch = 8;  // expert rows loaded before accumulating, combine
 
 struct Geometry {
   uint8_t* base;         // rank 0's buffer
@@ -47,6 +45,7 @@ struct Geometry {
   uint64_t sig_off;      // this set's signal words
   uint64_t msg;          // 4 + 2H
   int32_t* err;          // optional error word
+  uint32_t flags;        // LLMOE_FLAG_*
   int T_max, T, H, R, E, K, L;
   int nq;       // 16-byte quads per row, H / 8
   int nchunks;  // warp units per row, ceil(nq / 32)
@@ -57,6 +56,16 @@ struct Geometry {
 __device__ __forceinline__ void report(int32_t* err, int32_t code) {
   if (err != nullptr) atomicCAS(err, 0, code);
 }
+
+// Programmatic dependent launch: every kernel here is launched so that it may
+// start while the previous kernel on the stream drains.  Each kernel first
+// lets the next kernel on the stream begin launching (that kernel still waits
+// for this one before it touches memory), then waits for the previous grid to
+// complete and flush before its first global memory access (a no-op when
+// launched without the attribute).  With LLMOE_FLAG_INPUTS_READY, dispatch
+// and combine read their routing inputs before that wait.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void release_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Shared-memory view used by the three route-scan kernels.
 struct RouteSmem {
@@ -73,54 +82,66 @@ __device__ __forceinline__ RouteSmem carve_route(unsigned char* smem, const Geom
   return s;
 }
 
-// Routing count / prefix scan for tokens [t0, t1) of source rank src.
-// On return (after a __syncthreads): s.slot[q] for q = (t - t0) * K + k, and,
-// when full_counts, s.hist[e] = number of entries of src choosing e over all
-// of the call's tokens.
-__device__ void route_scan(const Geometry& g, const int64_t* __restrict__ idx, int src, int t0, int t1,
-                           bool full_counts, const RouteSmem& s) {
-  const int tid = threadIdx.x;
+// Routing count / prefix scan for tokens [t0, t1) of source rank src, in two
+// steps.  route_hist loads the block's entries into s.ent and builds s.hist =
+// per-expert entries of the tokens before the block (returns after a
+// __syncthreads).  route_slot(q) then gives entry q's slot: hist[e] plus the
+// earlier in-block tokens choosing e; each thread calls it for its own
+// entries, so a kernel can turn slots into addresses in the same pass.
+// route_count_block adds the block's entries to s.hist (full counts, for the
+// CTA of a source rank's last block); its caller syncs before reading them.
+constexpr int kPrefetch = 4;  // prefix ids each thread loads before the first barrier
+
+__device__ void route_hist(const Geometry& g, const int64_t* __restrict__ idx, int src, int t0, int t1,
+                           const RouteSmem& s) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
   const int K = g.K, E = g.E;
-  for (int e = tid; e < E; e += blockDim.x) s.hist[e] = 0;
   const int64_t* src_idx = idx + (int64_t)src * g.T * K;
-  const int nblock = (t1 - t0) * K;
-  for (int q = tid; q < nblock; q += blockDim.x) {
-    int64_t e = src_idx[(int64_t)t0 * K + q];
+  const int npre = t0 * K, nblock = (t1 - t0) * K;
+  // issue the prefix loads first: one memory latency for the whole prologue
+  int64_t pre[kPrefetch];
+#pragma unroll
+  for (int j = 0; j < kPrefetch; ++j) {
+    const int i = tid + j * nthr;
+    pre[j] = i < npre ? src_idx[i] : -1;
+  }
+  for (int e = tid; e < E; e += nthr) s.hist[e] = 0;
+  for (int q = tid; q < nblock; q += nthr) {
+    const int64_t e = src_idx[npre + q];
     s.ent[q] = (e >= 0 && e < E) ? (int)e : -1;
     if (e < -1 || e >= E) report(g.err, LLMOE_DEV_BAD_EXPERT);
   }
   __syncthreads();
-  // histogram of the tokens before the block
-  const int npre = t0 * K;
-  for (int i = tid; i < npre; i += blockDim.x) {
-    int64_t e = src_idx[i];
+#pragma unroll
+  for (int j = 0; j < kPrefetch; ++j)
+    if (pre[j] >= 0 && pre[j] < E) atomicAdd(&s.hist[pre[j]], 1);
+  for (int i = tid + kPrefetch * nthr; i < npre; i += nthr) {
+    const int64_t e = src_idx[i];
     if (e >= 0 && e < E) atomicAdd(&s.hist[e], 1);
   }
   __syncthreads();
-  // slot = earlier tokens before the block + earlier tokens inside it
-  for (int q = tid; q < nblock; q += blockDim.x) {
-    const int e = s.ent[q];
-    int sl = -1;
-    if (e >= 0) {
-      const int tl = q / K, k = q % K;
-      int r = 0;
-      for (int p = 0; p < tl * K; ++p) r += (s.ent[p] == e);
-      for (int k2 = 0; k2 < k; ++k2)
-        if (s.ent[tl * K + k2] == e) report(g.err, LLMOE_DEV_DUPLICATE);
-      sl = s.hist[e] + r;
-      if (sl >= g.T_max) {  // only reachable when a token repeats an expert
-        report(g.err, LLMOE_DEV_SLOT_RANGE);
-        sl = -1;
-      }
-    }
-    s.slot[q] = sl;
+}
+
+__device__ __forceinline__ int route_slot(const Geometry& g, const RouteSmem& s, int q) {
+  const int e = s.ent[q];
+  if (e < 0) return -1;
+  const int K = g.K, tl = q / K, k = q % K;
+  int r = 0;
+  for (int p = 0; p < tl * K; ++p) r += (s.ent[p] == e);
+  for (int k2 = 0; k2 < k; ++k2)
+    if (s.ent[tl * K + k2] == e) report(g.err, LLMOE_DEV_DUPLICATE);
+  const int sl = s.hist[e] + r;
+  if (sl >= g.T_max) {  // only reachable when a token repeats an expert
+    report(g.err, LLMOE_DEV_SLOT_RANGE);
+    return -1;
   }
-  __syncthreads();
-  if (full_counts) {
-    for (int q = tid; q < nblock; q += blockDim.x)
-      if (s.ent[q] >= 0) atomicAdd(&s.hist[s.ent[q]], 1);
-    __syncthreads();
-  }
+  return sl;
+}
+
+// After every thread's route_slot calls (i.e. after a __syncthreads).
+__device__ __forceinline__ void route_count_block(const RouteSmem& s, int nblock) {
+  for (int q = threadIdx.x; q < nblock; q += blockDim.x)
+    if (s.ent[q] >= 0) atomicAdd(&s.hist[s.ent[q]], 1);
 }
 
 // Writes rank dst's (dispatch) or rank src's (combine) signal words from the
@@ -128,17 +149,6 @@ __device__ void route_scan(const Geometry& g, const int64_t* __restrict__ idx, i
 __device__ __forceinline__ void put_signal(const Geometry& g, int64_t* word, int value) {
   if (g.err != nullptr && *reinterpret_cast<volatile int64_t*>(word) != 0) report(g.err, LLMOE_DEV_STALE_SIGNAL);
   *word = (int64_t)value;
-}
-
-__device__ __forceinline__ uint4 ldg16(const uint4* p) { return __ldg(p); }
-
-__device__ __forceinline__ uint4 shfl_up16(uint4 v, int lane_delta) {
-  uint4 r;
-  r.x = __shfl_up_sync(0xffffffffu, v.x, lane_delta);
-  r.y = __shfl_up_sync(0xffffffffu, v.y, lane_delta);
-  r.z = __shfl_up_sync(0xffffffffu, v.z, lane_delta);
-  r.w = __shfl_up_sync(0xffffffffu, v.w, lane_delta);
-  return r;
 }
 
 // Destination quad from the previous and current source quads when the
@@ -185,49 +195,213 @@ __device__ __forceinline__ void put_quad(uint8_t* msg_addr, int j, int nq, const
   }
 }
 
-__global__ void __launch_bounds__(kThreads) dispatch_kernel(Geometry g, const uint16_t* __restrict__ x,
-                                                            const int64_t* __restrict__ idx) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const RouteSmem s = carve_route(smem, g);
-  uint8_t** s_dst = reinterpret_cast<uint8_t**>(s.slot + g.TB * g.K + (g.E & 1));
+// ---------------------------------------------------------------------------
+// Asynchronous bulk copies into a shared-memory ring (cp.async.bulk with
+// mbarrier completion).  One producer lane keeps up to kStages chunks in
+// flight per CTA without holding them in registers; consumer warps wait on a
+// stage's "full" barrier, use it, and arrive on its "empty" barrier so the
+// producer can refill it.  Every wait is bounded (kSpinLimit clock cycles,
+// about one second): on expiry the kernel records LLMOE_DEV_TIMEOUT, stops
+// issuing, and drains the copies it has in flight before it returns.
+// ---------------------------------------------------------------------------
+constexpr long long kSpinLimit = 2000000000LL;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Waits for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - start > kSpinLimit) {
+      report(err, LLMOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// global -> shared bulk copy; both addresses 16-byte aligned, bytes % 16 == 0
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// The ring: kStages stages of stage_bytes each, plus full / empty barriers.
+template <int kStages>
+struct Ring {
+  uint8_t* data;
+  uint64_t* full;
+  uint64_t* empty;
+  uint32_t stage_bytes;
+  __device__ uint8_t* stage(int s) const { return data + (size_t)s * stage_bytes; }
+};
+
+// Producer-side bookkeeping shared with the drain at the end of a kernel.
+struct RingState {
+  int issued;    // stages handed to the copy engine
+  int consumed;  // lowest stage count every consumer warp got through
+};
+
+// After a timeout: wait (bounded) for every issued stage nobody consumed, so
+// no copy is still writing this CTA's shared memory when it exits.
+template <int kStages>
+__device__ void ring_drain(const Ring<kStages>& r, const RingState& st, int32_t* err) {
+  for (int it = st.consumed; it < st.issued; ++it) {
+    const int s = it % kStages;
+    if (!mbar_wait(&r.full[s], (it / kStages) & 1, err)) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dispatch
+// ---------------------------------------------------------------------------
+// Ring shapes (compile-time tuning parameters).
+#ifndef LLMOE_DSP_CONSUMERS
+#define LLMOE_DSP_CONSUMERS 4
+#endif
+#ifndef LLMOE_DSP_STAGES
+#define LLMOE_DSP_STAGES 8
+#endif
+#ifndef LLMOE_CMB_THREADS
+#define LLMOE_CMB_THREADS 128
+#endif
+
+constexpr int kDspConsumers = LLMOE_DSP_CONSUMERS;   // warps; lanes x 16 B = one chunk
+constexpr int kDspChunk = kDspConsumers * 32 * 16;   // x bytes per stage
+constexpr int kDspStageBytes = kDspChunk + 16;       // + the quad before the chunk
+constexpr int kDspStages = LLMOE_DSP_STAGES;
+constexpr int kDspThreads = 32 * (1 + kDspConsumers);
+
+__global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const uint16_t* __restrict__ x,
+                                                               const int64_t* __restrict__ idx) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  Ring<kDspStages> ring;
+  ring.data = smem;
+  ring.stage_bytes = kDspStageBytes;
+  ring.full = reinterpret_cast<uint64_t*>(smem + kDspStages * kDspStageBytes);
+  ring.empty = ring.full + kDspStages;
+  __shared__ RingState st;
+  const RouteSmem s = carve_route(reinterpret_cast<unsigned char*>(ring.empty + kDspStages), g);
+  uintptr_t* s_dst = reinterpret_cast<uintptr_t*>(s.slot + g.TB * g.K + (g.E & 1));
 
   const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
   const bool last = (b == g.nblk - 1);
-  route_scan(g, idx, src, t0, t1, last, s);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row_bytes = 2 * g.H;
+  const int nch = (row_bytes + kDspChunk - 1) / kDspChunk;
+  const int n_iters = (t1 - t0) * nch;
 
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDspStages; ++i) {
+      mbar_init(&ring.full[i], 1);
+      mbar_init(&ring.empty[i], kDspConsumers);
+    }
+    mbar_init_fence();
+    st.issued = 0;
+    st.consumed = INT_MAX;
+  }
+  const bool early = (g.flags & LLMOE_FLAG_INPUTS_READY) != 0;
+  release_next_grid();
+  if (!early) wait_prior_grid();
+
+  // x does not depend on the routing: start streaming it before the scan
+  const uint8_t* xsrc = reinterpret_cast<const uint8_t*>(x + ((int64_t)src * g.T + t0) * g.H);
+  auto issue = [&](int it) {
+    const int tl = it / nch, c = it % nch;
+    const int len = min(kDspChunk, row_bytes - c * kDspChunk);
+    uint8_t* dst = ring.stage(it % kDspStages);
+    const uint8_t* row = xsrc + (size_t)tl * row_bytes;
+    if (c == 0) {
+      mbar_arrive_expect_tx(&ring.full[it % kDspStages], len);
+      bulk_load(dst + 16, row, len, &ring.full[it % kDspStages]);
+    } else {
+      mbar_arrive_expect_tx(&ring.full[it % kDspStages], len + 16);
+      bulk_load(dst, row + c * kDspChunk - 16, len + 16, &ring.full[it % kDspStages]);
+    }
+  };
+  __syncthreads();  // barriers initialised
+  int next = 0;
+  if (threadIdx.x == 0)
+    for (; next < n_iters && next < kDspStages; ++next) issue(next);
+
+  route_hist(g, idx, src, t0, t1, s);
   const int nblock = (t1 - t0) * g.K;
   for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
-    const int e = s.ent[q], sl = s.slot[q];
-    uint8_t* d = nullptr;
-    if (e >= 0 && sl >= 0) {
+    const int e = s.ent[q], sl = route_slot(g, s, q);
+    uintptr_t d = 0;
+    if (sl >= 0) {
       const int dst = e / g.L, le = e % g.L;
       const uint64_t row = ((uint64_t)le * g.R + src) * g.T_max + sl;
-      d = g.base + dst * g.rank_stride + g.recv_off + row * g.msg;
+      d = reinterpret_cast<uintptr_t>(g.base + dst * g.rank_stride + g.recv_off + row * g.msg);
     }
     s_dst[q] = d;
   }
   __syncthreads();
+  if (early) wait_prior_grid();  // the receive rows and signal words may be in use until now
+  if (last) route_count_block(s, nblock);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nunits = (t1 - t0) * g.nchunks;
-  for (int u = warp; u < nunits; u += kWarps) {
-    const int tl = u / g.nchunks, c = u % g.nchunks;
-    const int t = t0 + tl;
-    const uint4* xrow = reinterpret_cast<const uint4*>(x + ((int64_t)src * g.T + t) * g.H);
-    const int j = c * 32 + lane;
-    uint4 cur = make_uint4(0, 0, 0, 0);
-    if (j < g.nq) cur = ldg16(xrow + j);
-    uint4 prev = shfl_up16(cur, 1);
-    if (lane == 0) prev = (j == 0) ? make_uint4(0, 0, 0, (uint32_t)t) : ldg16(xrow + j - 1);
-    if (j < g.nq) {
-      uint8_t* const* dsts = s_dst + tl * g.K;
-      for (int k = 0; k < g.K; ++k) {
-        uint8_t* d = dsts[k];
-        if (d != nullptr) put_quad(d, j, g.nq, prev, cur);
+  if (warp == 0) {
+    if (lane == 0) {
+      for (; next < n_iters; ++next) {
+        const int use = next / kDspStages;
+        if (!mbar_wait(&ring.empty[next % kDspStages], (use - 1) & 1, g.err)) break;
+        issue(next);
       }
+      st.issued = next;
     }
+  } else {
+    const int ct = threadIdx.x - 32;  // 0 .. 127: the 16-byte quad of the chunk
+    int it = 0;
+    for (; it < n_iters; ++it) {
+      const int sidx = it % kDspStages;
+      if (!mbar_wait(&ring.full[sidx], (it / kDspStages) & 1, g.err)) break;
+      const int tl = it / nch, c = it % nch;
+      const int len = min(kDspChunk, row_bytes - c * kDspChunk);
+      const uint8_t* sb = ring.stage(sidx);
+      if (ct * 16 < len) {
+        const uint4 cur = *reinterpret_cast<const uint4*>(sb + 16 + 16 * ct);
+        const uint4 prev = (c == 0 && ct == 0) ? make_uint4(0, 0, 0, (uint32_t)(t0 + tl))
+                                               : *reinterpret_cast<const uint4*>(sb + 16 * ct);
+        const int j = c * (kDspChunk / 16) + ct;
+        const uintptr_t* dsts = s_dst + tl * g.K;
+        for (int k = 0; k < g.K; ++k) {
+          const uintptr_t d = dsts[k];
+          if (d != 0) put_quad(reinterpret_cast<uint8_t*>(d), j, g.nq, prev, cur);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ring.empty[sidx]);
+    }
+    if (lane == 0) atomicMin(&st.consumed, it);
   }
+  __syncthreads();
+  if (st.consumed < st.issued) ring_drain(ring, st, g.err);
 
   if (last) {
     // rank dst's word le * R + src = count of bucket (le, src)
@@ -239,6 +413,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(Geometry g, const ui
   }
 }
 
+// ---------------------------------------------------------------------------
+// combine
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
@@ -258,11 +435,18 @@ __device__ __forceinline__ void axpy_quad(float (&acc)[8], float w, const uint4&
   acc[7] = __fadd_rn(acc[7], __fmul_rn(w, bf16hi(v.w)));
 }
 
-__global__ void __launch_bounds__(kThreads) combine_kernel(Geometry g, const uint16_t* __restrict__ y,
-                                                           const int64_t* __restrict__ idx,
-                                                           const float* __restrict__ topk_w,
-                                                           uint16_t* __restrict__ out) {
-  extern __shared__ __align__(16) unsigned char smem[];
+// One warp reduces 32 quads (512 B) of one output row per unit: up to
+// kKBatch expert rows are loaded (16 B per lane each) before they are
+// accumulated, in ascending k.
+constexpr int kCmbThreads = LLMOE_CMB_THREADS;
+constexpr int kCmbWarps = kCmbThreads / 32;
+constexpr int kKBatch = 8;
+
+__global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const uint16_t* __restrict__ y,
+                                                              const int64_t* __restrict__ idx,
+                                                              const float* __restrict__ topk_w,
+                                                              uint16_t* __restrict__ out) {
+  extern __shared__ __align__(128) unsigned char smem[];
   const RouteSmem s = carve_route(smem, g);
   const int TBK = g.TB * g.K;
   const uint4** s_row = reinterpret_cast<const uint4**>(s.slot + TBK + (g.E & 1));
@@ -271,24 +455,31 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Geometry g, const uin
   const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
   const bool last = (b == g.nblk - 1);
-  route_scan(g, idx, src, t0, t1, last, s);
-
   const int nblock = (t1 - t0) * g.K;
+  const float* wblk = topk_w + ((int64_t)src * g.T + t0) * g.K;
+  const bool early = (g.flags & LLMOE_FLAG_INPUTS_READY) != 0;
+  release_next_grid();
+  if (!early) wait_prior_grid();
+  const float w0 = threadIdx.x < nblock ? wblk[threadIdx.x] : 0.0f;  // before the prologue's barriers
+
+  route_hist(g, idx, src, t0, t1, s);
   for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
-    const int e = s.ent[q], sl = s.slot[q];
+    const int e = s.ent[q], sl = route_slot(g, s, q);
     const uint4* r = nullptr;
-    if (e >= 0 && sl >= 0) {
+    if (sl >= 0) {
       const uint64_t row = (uint64_t)e * g.R * g.T_max + (uint64_t)src * g.T_max + sl;
       r = reinterpret_cast<const uint4*>(y + row * g.H);
     }
     s_row[q] = r;
-    s_w[q] = topk_w[((int64_t)src * g.T + t0) * g.K + q];
+    s_w[q] = q == threadIdx.x ? w0 : wblk[q];
   }
   __syncthreads();
+  if (early) wait_prior_grid();  // y and the signal words may come from the previous kernel
+  if (last) route_count_block(s, nblock);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nunits = (t1 - t0) * g.nchunks;
-  for (int u = warp; u < nunits; u += kWarps) {
+  for (int u = warp; u < nunits; u += kCmbWarps) {
     const int tl = u / g.nchunks, c = u % g.nchunks;
     const int t = t0 + tl;
     const int j = c * 32 + lane;
@@ -304,7 +495,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Geometry g, const uin
       for (int i = 0; i < kKBatch; ++i) {
         const int k = k0 + i;
         v[i] = make_uint4(0, 0, 0, 0);
-        if (k < g.K && rows[k] != nullptr) v[i] = ldg16(rows[k] + j);
+        if (k < g.K && rows[k] != nullptr) v[i] = __ldg(rows[k] + j);
       }
 #pragma unroll
       for (int i = 0; i < kKBatch; ++i) {
@@ -321,6 +512,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Geometry g, const uin
   }
 
   if (last) {
+    __syncthreads();
     // rank src's word e = rows expert e returns to src
     int64_t* w = reinterpret_cast<int64_t*>(g.base + src * g.rank_stride + g.sig_off);
     for (int e = threadIdx.x; e < g.E; e += blockDim.x) put_signal(g, w + e, s.hist[e]);
@@ -330,22 +522,30 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Geometry g, const uin
 __global__ void __launch_bounds__(kThreads) route_kernel(Geometry g, const int64_t* __restrict__ idx,
                                                          int32_t* __restrict__ slot_out,
                                                          int64_t* __restrict__ counts) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   const RouteSmem s = carve_route(smem, g);
   const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
   const bool last = (b == g.nblk - 1);
-  route_scan(g, idx, src, t0, t1, last, s);
+  release_next_grid();
+  wait_prior_grid();
+  route_hist(g, idx, src, t0, t1, s);
   const int nblock = (t1 - t0) * g.K;
   for (int q = threadIdx.x; q < nblock; q += blockDim.x)
-    slot_out[((int64_t)src * g.T + t0) * g.K + q] = s.slot[q];
-  if (last)
+    slot_out[((int64_t)src * g.T + t0) * g.K + q] = route_slot(g, s, q);
+  if (last) {
+    __syncthreads();
+    route_count_block(s, nblock);
+    __syncthreads();
     for (int e = threadIdx.x; e < g.E; e += blockDim.x) counts[(int64_t)e * g.R + src] = s.hist[e];
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) clean_kernel(uint8_t* base, uint64_t rank_stride, uint64_t sig_off,
                                                          int R, int E) {
   const int64_t n = (int64_t)R * E;
+  release_next_grid();
+  wait_prior_grid();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / E, e = i % E;
     reinterpret_cast<int64_t*>(base + r * rank_stride + sig_off)[e] = 0;
@@ -427,6 +627,7 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   g->sig_off = 2 * li.send + 2 * li.recv + li.sig * (uint64_t)set;
   g->msg = li.msg;
   g->err = bs->err;
+  g->flags = bs->flags;
   g->T_max = T_max;
   g->T = T;
   g->H = H;
@@ -436,15 +637,57 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   g->L = E / R;
   g->nq = H / 8;
   g->nchunks = (g->nq + 31) / 32;
-  // tokens per CTA: enough CTAs for about 8 resident per SM, at most 32 tokens
-  const int64_t tokens = (int64_t)R * T;
-  const int64_t target = (int64_t)num_sms() * 8;
-  int64_t tb = (tokens + target - 1) / target;
+  g->TB = 1;
+  g->nblk = T > 0 ? T : 1;
+  return LLMOE_SUCCESS;
+}
+
+// Tokens per CTA: the fewest that keep the grid within one wave of resident
+// CTAs (SMs x blocks_per_sm), at most kMaxTokensPerBlock.
+void set_blocking(Geometry* g, int blocks_per_sm) {
+  const int64_t tokens = (int64_t)g->R * g->T;
+  const int64_t wave = (int64_t)num_sms() * (blocks_per_sm > 0 ? blocks_per_sm : 1);
+  int64_t tb = (tokens + wave - 1) / wave;
   if (tb < 1) tb = 1;
   if (tb > kMaxTokensPerBlock) tb = kMaxTokensPerBlock;
   g->TB = (int)tb;
-  g->nblk = T > 0 ? (T + g->TB - 1) / g->TB : 1;
+  g->nblk = g->T > 0 ? (g->T + g->TB - 1) / g->TB : 1;
+}
+
+int g_smem_optin[64][3] = {{0}};
+
+// Opts a kernel in to more than 48 KB of dynamic shared memory (once per
+// device and size).
+int set_smem(int id, const void* fn, size_t bytes) {
+  if (bytes <= 48 * 1024) return LLMOE_SUCCESS;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LLMOE_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && (size_t)g_smem_optin[dev][id] >= bytes) return LLMOE_SUCCESS;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return LLMOE_ERR_CUDA;
+  }
+  if (dev >= 0 && dev < 64) g_smem_optin[dev][id] = (int)bytes;
   return LLMOE_SUCCESS;
+}
+
+enum KernelId { kRouteKernel = 0, kDispatchKernel = 1, kCombineKernel = 2, kNumKernels = 3 };
+int g_occupancy[64][kNumKernels] = {{0}};
+
+// Resident CTAs per SM of a kernel at kThreads threads and `smem` bytes,
+// cached per device.
+int blocks_per_sm(KernelId id, const void* fn, int threads, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < 64 && g_occupancy[dev][id] > 0) return g_occupancy[dev][id];
+  int n = 0;
+  if (set_smem(id, fn, smem) != LLMOE_SUCCESS) return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  if (dev < 64) g_occupancy[dev][id] = n;
+  return n;
 }
 
 size_t route_smem_bytes(const Geometry& g) {
@@ -452,14 +695,35 @@ size_t route_smem_bytes(const Geometry& g) {
   return sizeof(int) * ((size_t)g.E + 2 * tbk + (size_t)(g.E & 1));  // pad: 8-byte arrays follow
 }
 
-int set_smem(const void* fn, size_t bytes) {
-  if (bytes <= 48 * 1024) return LLMOE_SUCCESS;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
-    return LLMOE_ERR_CUDA;
-  return LLMOE_SUCCESS;
+size_t dispatch_smem_bytes(const Geometry& g) {
+  return (size_t)kDspStages * kDspStageBytes + 2 * kDspStages * sizeof(uint64_t) + route_smem_bytes(g) +
+         sizeof(uintptr_t) * (size_t)g.TB * g.K;
 }
 
-int launch_status() { return cudaGetLastError() == cudaSuccess ? LLMOE_SUCCESS : LLMOE_ERR_CUDA; }
+size_t combine_smem_bytes(const Geometry& g) {
+  return route_smem_bytes(g) + (sizeof(void*) + sizeof(float)) * (size_t)g.TB * g.K;
+}
+
+// Launches with programmatic stream serialization (see wait_prior_grid).
+template <typename... KArgs, typename... Args>
+int launch(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, llmoe_stream_t stream,
+           Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
+    cudaGetLastError();  // clear the launch error so it does not leak into later calls
+    return LLMOE_ERR_CUDA;
+  }
+  return LLMOE_SUCCESS;
+}
 
 }  // namespace
 
@@ -489,10 +753,10 @@ int llmoe_route(const int64_t* topk_idx, int32_t* slot, int64_t* counts, const l
   if (counts == nullptr || !aligned(counts, 8)) return LLMOE_ERR_INVALID_ARGUMENT;
   if (g.T > 0 && (topk_idx == nullptr || slot == nullptr || !aligned(topk_idx, 8) || !aligned(slot, 4)))
     return LLMOE_ERR_INVALID_ARGUMENT;
+  set_blocking(&g, blocks_per_sm(kRouteKernel, (const void*)route_kernel, kThreads, route_smem_bytes(g)));
   const size_t smem = route_smem_bytes(g);
-  if ((rc = set_smem((const void*)route_kernel, smem)) != LLMOE_SUCCESS) return rc;
-  route_kernel<<<g.R * g.nblk, kThreads, smem, (cudaStream_t)stream>>>(g, topk_idx, slot, counts);
-  return launch_status();
+  if ((rc = set_smem(kRouteKernel, (const void*)route_kernel, smem)) != LLMOE_SUCCESS) return rc;
+  return launch(route_kernel, g.R * g.nblk, kThreads, smem, stream, g, topk_idx, slot, counts);
 }
 
 int llmoe_dispatch(const uint16_t* x, const int64_t* topk_idx, const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
@@ -501,11 +765,10 @@ int llmoe_dispatch(const uint16_t* x, const int64_t* topk_idx, const llmoe_buf_s
   if (rc != LLMOE_SUCCESS) return rc;
   if (g.T > 0 && (x == nullptr || topk_idx == nullptr || !aligned(x, 16) || !aligned(topk_idx, 8)))
     return LLMOE_ERR_INVALID_ARGUMENT;
-  const size_t tbk = (size_t)g.TB * g.K;
-  const size_t smem = route_smem_bytes(g) + sizeof(void*) * tbk;
-  if ((rc = set_smem((const void*)dispatch_kernel, smem)) != LLMOE_SUCCESS) return rc;
-  dispatch_kernel<<<g.R * g.nblk, kThreads, smem, (cudaStream_t)stream>>>(g, x, topk_idx);
-  return launch_status();
+  set_blocking(&g, blocks_per_sm(kDispatchKernel, (const void*)dispatch_kernel, kDspThreads, dispatch_smem_bytes(g)));
+  const size_t smem = dispatch_smem_bytes(g);
+  if ((rc = set_smem(kDispatchKernel, (const void*)dispatch_kernel, smem)) != LLMOE_SUCCESS) return rc;
+  return launch(dispatch_kernel, g.R * g.nblk, kDspThreads, smem, stream, g, x, topk_idx);
 }
 
 int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
@@ -522,11 +785,10 @@ int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const float* topk_
     const uintptr_t ye = yb + (uintptr_t)g.E * g.R * g.T_max * g.H * 2, oe = ob + (uintptr_t)g.R * g.T * g.H * 2;
     if (ob < ye && yb < oe) return LLMOE_ERR_INVALID_ARGUMENT;
   }
-  const size_t tbk = (size_t)g.TB * g.K;
-  const size_t smem = route_smem_bytes(g) + (sizeof(void*) + sizeof(float)) * tbk;
-  if ((rc = set_smem((const void*)combine_kernel, smem)) != LLMOE_SUCCESS) return rc;
-  combine_kernel<<<g.R * g.nblk, kThreads, smem, (cudaStream_t)stream>>>(g, y, topk_idx, topk_w, out);
-  return launch_status();
+  set_blocking(&g, blocks_per_sm(kCombineKernel, (const void*)combine_kernel, kCmbThreads, combine_smem_bytes(g)));
+  const size_t smem = combine_smem_bytes(g);
+  if ((rc = set_smem(kCombineKernel, (const void*)combine_kernel, smem)) != LLMOE_SUCCESS) return rc;
+  return launch(combine_kernel, g.R * g.nblk, kCmbThreads, smem, stream, g, y, topk_idx, topk_w, out);
 }
 
 int llmoe_clean(const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
@@ -536,8 +798,7 @@ int llmoe_clean(const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
   const int64_t n = (int64_t)g.R * g.E;
   int blocks = (int)((n + kThreads - 1) / kThreads);
   if (blocks > 64) blocks = 64;
-  clean_kernel<<<blocks, kThreads, 0, (cudaStream_t)stream>>>(g.base, g.rank_stride, g.sig_off, g.R, g.E);
-  return launch_status();
+  return launch(clean_kernel, blocks, kThreads, 0, stream, g.base, g.rank_stride, g.sig_off, g.R, g.E);
 }
 
 int llmoe_get_error(const llmoe_buf_set_t* bs, llmoe_stream_t stream, int32_t* code, int reset) {

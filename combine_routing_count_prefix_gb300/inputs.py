@@ -22,6 +22,10 @@ dsv3           8   128   7168   256  8  DeepSeek-V3-shaped decode; uniform
 skewed         8   128   4096   64   6  Zipf(1.2) w/o replacement, 10% -1
 many_small     32  16    2048   128  4  uniform; x ~ U(-1,1)
 large          8   1024  7168   256  8  uniform; worst-case layout ~120 GB
+dense16        8   256   7168   16   8  uniform; small layout (2.4 GB with
+                                        y), kernel traffic above L2 size:
+                                        the profiling case for the dsv3
+                                        kernels (same row length and top-k)
 =============  ==  ====  =====  ===  =  ====================================
 
 Expert outputs ``y`` are the dense [E * R * T_max, H] bf16 matrix the combine
@@ -74,6 +78,7 @@ WORKLOADS = {
     "skewed": Workload("skewed", 8, 128, 4096, 64, 6, routing="zipf", zipf_s=1.2, mask_p=0.10),
     "many_small": Workload("many_small", 32, 16, 2048, 128, 4, x_dist="uniform"),
     "large": Workload("large", 8, 1024, 7168, 256, 8),
+    "dense16": Workload("dense16", 8, 256, 7168, 16, 8),
 }
 
 

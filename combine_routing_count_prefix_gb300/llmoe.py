@@ -32,6 +32,9 @@ LLMOE_DEV_BAD_EXPERT = 1
 LLMOE_DEV_DUPLICATE = 2
 LLMOE_DEV_STALE_SIGNAL = 3
 LLMOE_DEV_SLOT_RANGE = 4
+LLMOE_DEV_TIMEOUT = 5
+
+LLMOE_FLAG_INPUTS_READY = 1
 
 LLMOE_MAX_TOPK = 32
 LLMOE_MAX_EXPERTS = 8192
@@ -52,6 +55,7 @@ class llmoe_buf_set_t(ctypes.Structure):
         ("num_topk", ctypes.c_int32),
         ("set", ctypes.c_int32),
         ("err", ctypes.c_void_p),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -161,6 +165,39 @@ def llmoe_get_error(bs: llmoe_buf_set_t, stream=None, reset: bool = False) -> in
     return code.value
 
 
+class Bound:
+    """One C-ABI call with its arguments marshalled once, for tight loops:
+    calling it issues the call and raises on a non-zero status."""
+
+    __slots__ = ("fn", "args", "name", "keep")
+
+    def __init__(self, name: str, args: tuple, keep=()):
+        self.fn = getattr(_lib, name)
+        self.args = args
+        self.name = name
+        self.keep = keep  # objects the marshalled pointers refer to
+
+    def __call__(self) -> None:
+        rc = self.fn(*self.args)
+        if rc != LLMOE_SUCCESS:
+            raise LLMoEError(rc, self.name)
+
+
+def bind_dispatch(x, topk_idx, bs: llmoe_buf_set_t, stream=None) -> Bound:
+    return Bound("llmoe_dispatch", (_addr(x, "bf16"), _addr(topk_idx, "i64"), ctypes.byref(bs), _stream(stream)),
+                 (x, topk_idx, bs))
+
+
+def bind_combine(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=None) -> Bound:
+    return Bound("llmoe_combine", (_addr(y, "bf16"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"),
+                                   _addr(out, "bf16"), ctypes.byref(bs), _stream(stream)),
+                 (y, topk_idx, topk_w, out, bs))
+
+
+def bind_clean(bs: llmoe_buf_set_t, stream=None) -> Bound:
+    return Bound("llmoe_clean", (ctypes.byref(bs), _stream(stream)), (bs,))
+
+
 def round_up(v: int, a: int) -> int:
     return (v + a - 1) // a * a
 
@@ -188,11 +225,13 @@ class RankBuffers:
     def msg_bytes(self) -> int:
         return 4 + 2 * self.H
 
-    def buf_set(self, set: int, num_topk: int, num_tokens: int | None = None, err=None) -> llmoe_buf_set_t:
+    def buf_set(self, set: int, num_topk: int, num_tokens: int | None = None, err=None,
+                flags: int = 0) -> llmoe_buf_set_t:
         return llmoe_buf_set_t(
             base=self.storage.data_ptr(), rank_stride=self.rank_stride, num_max_tokens=self.T,
             num_tokens=self.T if num_tokens is None else num_tokens, hidden=self.H, num_ranks=self.R,
-            num_experts=self.E, num_topk=num_topk, set=set, err=None if err is None else _addr(err, "i32"))
+            num_experts=self.E, num_topk=num_topk, set=set, err=None if err is None else _addr(err, "i32"),
+            flags=flags)
 
     def rank_view(self, r: int) -> torch.Tensor:
         return self.storage[r * self.rank_stride:(r + 1) * self.rank_stride]

@@ -69,6 +69,17 @@ typedef enum {
 #define LLMOE_DEV_DUPLICATE 2    /* one expert twice in one token's top-k */
 #define LLMOE_DEV_STALE_SIGNAL 3 /* a signal word was non-zero on entry (a clean was skipped) */
 #define LLMOE_DEV_SLOT_RANGE 4   /* a bucket overflowed num_max_tokens (only reachable with duplicates) */
+#define LLMOE_DEV_TIMEOUT 5      /* a bounded wait inside a kernel expired (a copy never completed) */
+
+/* llmoe_buf_set_t.flags */
+/* The call's read-only routing inputs (topk_idx and topk_w, and x for a
+ * dispatch) were complete before the kernel that precedes this call on the
+ * stream started, so the call's kernel may read them (and run its routing
+ * scan) while that kernel drains.  The expert outputs y of a combine, the
+ * rank buffers and the output are never touched before the preceding kernel
+ * has completed.  Typical use: a combine whose topk_idx / topk_w came from a
+ * router that ran before the expert kernels. */
+#define LLMOE_FLAG_INPUTS_READY 1u
 
 /* Library limits (checked on the host). */
 #define LLMOE_MAX_TOPK 32
@@ -91,7 +102,8 @@ typedef enum {
  *   set            0 or 1: which of the layout's two buffer sets.
  *   err            optional device int32 word; NULL turns validation off.
  *                  With validation off, invalid ids are still skipped and no
- *                  access leaves the buffers, but nothing is reported. */
+ *                  access leaves the buffers, but nothing is reported.
+ *   flags          LLMOE_FLAG_* bits; 0 for the plain stream order. */
 typedef struct {
   void* base;
   uint64_t rank_stride;
@@ -103,6 +115,7 @@ typedef struct {
   int32_t num_topk;
   int32_t set;
   int32_t* err;
+  uint32_t flags;
 } llmoe_buf_set_t;
 
 /* Bytes of ONE rank buffer: get_rdma_size_hint<bf16>(num_max_tokens, hidden,

@@ -363,3 +363,48 @@ def test_invalid_call_launches_nothing(L):
     assert ei.value.status == L.LLMOE_ERR_INVALID_ARGUMENT
     torch.cuda.synchronize()
     assert all_equal_chunked(r.rb.storage, CANARY)
+
+
+# ---------------------------------------------------------------------------
+# LLMOE_FLAG_INPUTS_READY: routing read before the previous kernel drains
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "skewed", "dsv3"])
+def test_inputs_ready_flag_same_results(L, name):
+    w = WORKLOADS[name]
+    r = Round(L, w, seed=12)
+    r.bs_d = r.rb.buf_set(r.ds, w.K, r.T_call, r.err, flags=L.LLMOE_FLAG_INPUTS_READY)
+    r.bs_c = r.rb.buf_set(r.cs, w.K, r.T_call, r.err, flags=L.LLMOE_FLAG_INPUTS_READY)
+    full_check(r)
+
+
+def test_inputs_ready_flag_in_cuda_graph_after_producer(L):
+    # the combine's y is written by the kernel right before it: the flag must
+    # still make the combine wait for y (only the routing is read early)
+    w = WORKLOADS["many_small"]
+    r = Round(L, w, seed=13)
+    r.bs_c = r.rb.buf_set(r.cs, w.K, r.T_call, r.err, flags=L.LLMOE_FLAG_INPUTS_READY)
+    y_final = r.y.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        r.run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        L.llmoe_clean(r.bs_d)
+        L.llmoe_dispatch(r.x, r.idx, r.bs_d)
+        L.llmoe_clean(r.bs_c)
+        r.y.copy_(y_final)  # the expert outputs land right before the combine
+        L.llmoe_combine(r.y, r.idx, r.wt, r.out, r.bs_c)
+    for _ in range(3):
+        r.y.zero_()
+        r.rb.storage.fill_(CANARY)
+        r.out.fill_(OUT_CANARY)
+        g.replay()
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    d = r.check_dispatch()
+    r.check_combine()
+    r.check_canary(d)
