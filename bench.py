@@ -2,7 +2,10 @@
 """Benchmark: microseconds per dispatch + combine round on one GB300.
 
 A step is one round on one batch of synthetic input, through the C ABI:
-    llmoe_clean(set 0); llmoe_dispatch(set 0); llmoe_clean(set 1); llmoe_combine(set 1)
+    llmoe_dispatch(set 0); llmoe_combine(set 1)
+with each call also zeroing the other buffer set's signal words (the two
+llmoe_clean calls of a round, fused into the data kernels); the same round as
+four separate calls (clean, dispatch, clean, combine) is reported beside it,
 on the DeepSeek-V3-shaped decode workload (R=8 simulated ranks, T=128 tokens
 per rank, H=7168 bf16, E=256 experts, top-8, uniform routing) unless
 --workload says otherwise.  Inputs are resident in HBM; L2 is flushed before
@@ -292,10 +295,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     y = dev(inp["y_pool"]).index_select(0, dev(inp["y_row_map"])).contiguous()
     out = torch.empty((w.R, tokens, w.H), dtype=torch.int16, device="cuda")
     rb = llmoe.RankBuffers(w.T, w.H, w.R, w.E, fill=0)
-    # the combine's routing (topk_idx, topk_w) is ready long before the kernel
-    # that precedes it, as in a MoE layer where the router ran before the
-    # experts: the combine may scan it while that kernel drains
-    bs0, bs1 = rb.buf_set(0, w.K), rb.buf_set(1, w.K, flags=llmoe.LLMOE_FLAG_INPUTS_READY)
+    # a round is dispatch(set 0) + combine(set 1) with each kernel also
+    # zeroing the other set's signal words (the cleans the next calls need,
+    # fused: LLMOE_FLAG_CLEAN_OTHER_SET); the combine's routing is ready long
+    # before the kernel that precedes it, as in a MoE layer whose router ran
+    # before the experts, so it is scanned while that kernel drains
+    # (LLMOE_FLAG_INPUTS_READY)
+    F = llmoe.LLMOE_FLAG_CLEAN_OTHER_SET
+    bs0 = rb.buf_set(0, w.K, flags=F)
+    bs1 = rb.buf_set(1, w.K, flags=F | llmoe.LLMOE_FLAG_INPUTS_READY)
+    # the same round as four calls with separate cleans
+    bs0_plain, bs1_plain = rb.buf_set(0, w.K), rb.buf_set(1, w.K, flags=llmoe.LLMOE_FLAG_INPUTS_READY)
     # L2 flush between timed steps: write a buffer larger than L2, then read
     # another one so the written lines are evicted (and written back) before
     # the step's first event instead of inside the step
@@ -307,60 +317,74 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         flush_r.sum()
 
     stream = torch.cuda.current_stream()
-    # the four C-ABI calls of a round, arguments marshalled once
-    clean0, clean1 = llmoe.bind_clean(bs0, stream), llmoe.bind_clean(bs1, stream)
+    # the C-ABI calls of a round, arguments marshalled once
     dispatch = llmoe.bind_dispatch(x, idx, bs0, stream)
     combine = llmoe.bind_combine(y, idx, wt, out, bs1, stream)
+    clean0, clean1 = llmoe.bind_clean(bs0_plain, stream), llmoe.bind_clean(bs1_plain, stream)
+    dispatch_plain = llmoe.bind_dispatch(x, idx, bs0_plain, stream)
+    combine_plain = llmoe.bind_combine(y, idx, wt, out, bs1_plain, stream)
 
     def step():
-        clean0()
         dispatch()
-        clean1()
         combine()
 
+    def step_four_calls():
+        clean0()
+        dispatch_plain()
+        clean1()
+        combine_plain()
+
+    clean0()  # once, before the first round
     for _ in range(args.warmup):
         flush()
         step()
+    for _ in range(3):
+        step_four_calls()
+    clean0()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
 
-    # pass A (value): events around each whole round only, so consecutive
-    # kernels overlap their launch with the previous kernel's drain
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    # pass B (roofline): events around every kernel
-    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    def new_events(n, k):
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
+
+    ev, ev4, evk = new_events(args.steps, 2), new_events(args.steps, 2), new_events(args.steps, 3)
     with ClockSampler(gpu_id_for(local_rank)) as clocks:
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         wall0 = time.perf_counter()
-        for a, b in ev:
+        # timed region (value): events around each round only, so the two
+        # kernels overlap their launch with the previous kernel's drain
+        for e in ev:
             flush()
-            a.record(stream)
+            e[0].record(stream)
             step()
-            b.record(stream)
+            e[1].record(stream)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         wall = time.perf_counter() - wall0
+        # the four-call round
+        for e in ev4:
+            flush()
+            e[0].record(stream)
+            step_four_calls()
+            e[1].record(stream)
+        clean0()
+        # events around every kernel (roofline)
         for e in evk:
             flush()
             e[0].record(stream)
-            clean0()
-            e[1].record(stream)
             dispatch()
-            e[2].record(stream)
-            clean1()
-            e[3].record(stream)
+            e[1].record(stream)
             combine()
-            e[4].record(stream)
+            e[2].record(stream)
         torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    disp_ms = [e[1].elapsed_time(e[2]) for e in evk]
-    comb_ms = [e[3].elapsed_time(e[4]) for e in evk]
-    clean_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evk]
-    round_b_ms = [e[0].elapsed_time(e[4]) for e in evk]
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    four_ms = [e[0].elapsed_time(e[1]) for e in ev4]
+    disp_ms = [e[0].elapsed_time(e[1]) for e in evk]
+    comb_ms = [e[1].elapsed_time(e[2]) for e in evk]
     timed = torch.tensor([sum(step_ms), wall], dtype=torch.float64, device="cuda")
     if world > 1:
         dist.all_reduce(timed, op=dist.ReduceOp.MAX)
@@ -391,23 +415,23 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "unmasked_entries": n_valid, "parallelism": f"replicas{world}",
                        "l2": f"flushed before every timed step, outside the events ({FLUSH_BYTES >> 20} MB write, "
                              f"then {FLUSH_READ_BYTES >> 20} MB read so the written lines leave L2 first)",
-                       "timing": "value: CUDA events around each round (pass A); per-kernel times and roofline: "
-                                 "events around every kernel (pass B, same step count)",
-                       "flags": "combine: LLMOE_FLAG_INPUTS_READY (routing scanned while the previous kernel "
-                                "drains); dispatch: none"},
+                       "round": "llmoe_dispatch(set 0) + llmoe_combine(set 1), each zeroing the other set's "
+                                "signal words (LLMOE_FLAG_CLEAN_OTHER_SET: the llmoe_clean calls fused); combine "
+                                "with LLMOE_FLAG_INPUTS_READY; round_us_four_calls: clean, dispatch, clean, "
+                                "combine as four calls",
+                       "timing": "value: CUDA events around each round; per-kernel times and roofline: a second "
+                                 "pass with events around every kernel, same step count"},
             "effective_gbs": round(gbs, 1), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
             "frac_of_measured_hbm": round(gbs / peak, 4),
             "algorithmic_bytes_per_round": algo["round"],
             "dispatch_us": round(d_us, 3), "combine_us": round(c_us, 3),
-            "clean_us": round(statistics.mean(clean_ms) * 1e3 / 2, 3),
-            "round_us_kernel_events": round(statistics.mean(round_b_ms) * 1e3, 3),
+            "round_us_four_calls": round(statistics.mean(four_ms) * 1e3, 3),
             "step_us_median": round(statistics.median(step_ms) * 1e3, 3),
             "wall_s": round(float(timed[1]), 3),
             "roofline": {"kernel": dom + "_kernel", "bound": "hbm", "achieved": round(dom_gbs, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                          "traffic": traffic, "algorithmic_bytes": algo[dom]},
-            "gpu_launches": 4 * args.steps,
-            "gpu_launches_kernel_pass": 4 * args.steps,
+            "gpu_launches": 2 * args.steps,
             "clocks": clocks.summary(),
         }
         if e2e is not None:
@@ -434,21 +458,22 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
         hw, device="cuda")
     dy = torch.empty_like(hy, device="cuda")
     dout = torch.empty_like(hout, device="cuda")
-    bs0, bs1 = rb.buf_set(0, w.K), rb.buf_set(1, w.K, flags=llmoe.LLMOE_FLAG_INPUTS_READY)
+    F = llmoe.LLMOE_FLAG_CLEAN_OTHER_SET
+    bs0 = rb.buf_set(0, w.K, flags=F)
+    bs1 = rb.buf_set(1, w.K, flags=F | llmoe.LLMOE_FLAG_INPUTS_READY)
     h2d = sum(t.numel() * t.element_size() for t in (hx, hidx, hw, hy))
     d2h = hout.numel() * hout.element_size() + hsig.numel() * hsig.element_size()
 
     def step():
         for d, h in ((dx, hx), (didx, hidx), (dw, hw), (dy, hy)):
             d.copy_(h, non_blocking=True)
-        llmoe.llmoe_clean(bs0, stream)
         llmoe.llmoe_dispatch(dx, didx, bs0, stream)
-        llmoe.llmoe_clean(bs1, stream)
         llmoe.llmoe_combine(dy, didx, dw, dout, bs1, stream)
         hout.copy_(dout, non_blocking=True)
         hsig[0].copy_(rb.signal_words(0), non_blocking=True)
         hsig[1].copy_(rb.signal_words(1), non_blocking=True)
 
+    llmoe.llmoe_clean(rb.buf_set(0, w.K), stream)
     for _ in range(3):
         step()
     torch.cuda.synchronize()

@@ -43,6 +43,7 @@ struct Geometry {
   uint64_t rank_stride;  // bytes between rank buffers
   uint64_t recv_off;     // this set's receive region, from a rank buffer's start
   uint64_t sig_off;      // this set's signal words
+  uint64_t other_sig_off;  // the other set's signal words
   uint64_t msg;          // 4 + 2H
   int32_t* err;          // optional error word
   uint32_t flags;        // LLMOE_FLAG_*
@@ -144,6 +145,18 @@ __device__ __forceinline__ void route_count_block(const RouteSmem& s, int nblock
     if (s.ent[q] >= 0) atomicAdd(&s.hist[s.ent[q]], 1);
 }
 
+// LLMOE_FLAG_CLEAN_OTHER_SET: the grid zeroes the other buffer set's R * E
+// signal words (the clean that the next call on that set needs), after it
+// has waited for the previous kernel.
+__device__ __forceinline__ void clean_other_set(const Geometry& g) {
+  if ((g.flags & LLMOE_FLAG_CLEAN_OTHER_SET) == 0) return;
+  const int64_t n = (int64_t)g.R * g.E;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / g.E, e = i % g.E;
+    reinterpret_cast<int64_t*>(g.base + r * g.rank_stride + g.other_sig_off)[e] = 0;
+  }
+}
+
 // Writes rank dst's (dispatch) or rank src's (combine) signal words from the
 // full histogram; checks that each word was zero (cleaned) in validate mode.
 __device__ __forceinline__ void put_signal(const Geometry& g, int64_t* word, int value) {
@@ -169,12 +182,19 @@ __device__ __forceinline__ void st8(uint8_t* p, uint32_t a, uint32_t b) {
 __device__ __forceinline__ void st4(uint8_t* p, uint32_t a) { *reinterpret_cast<uint32_t*>(p) = a; }
 
 // Writes source quad j of a token row (and the header / tail pieces that fall
-// to it) into the message at `msg_addr`.  prev is quad j-1, or (0,0,0,t) for
-// j == 0 so that prev.w is the header.
-__device__ __forceinline__ void put_quad(uint8_t* msg_addr, int j, int nq, const uint4& prev, const uint4& cur) {
-  uint8_t* pa = msg_addr + 4;  // payload
-  const int phase = (int)((reinterpret_cast<uintptr_t>(pa) >> 2) & 3);
-  uint8_t* qb = pa - 4 * phase;  // 16-byte aligned
+// to it) into the message at `dest` (pack_dest).  prev is quad j-1, or
+// (0,0,0,t) for j == 0 so that prev.w is the header.
+// A message destination packed into one word: the 16-byte-aligned address
+// qb at or below the payload start, OR the payload's 4-byte phase (0..3).
+__device__ __forceinline__ uintptr_t pack_dest(uint8_t* msg_addr) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(msg_addr) + 4;
+  return (pa & ~(uintptr_t)15) | ((pa >> 2) & 3);
+}
+
+__device__ __forceinline__ void put_quad(uintptr_t dest, int j, int nq, const uint4& prev, const uint4& cur) {
+  const int phase = (int)(dest & 3);
+  uint8_t* qb = reinterpret_cast<uint8_t*>(dest & ~(uintptr_t)15);  // 16-byte aligned
+  uint8_t* pa = qb + 4 * phase;                                       // payload
   if (j > 0) {
     st16(qb + 16 * j, shift_words(prev, cur, phase));
   } else {
@@ -296,6 +316,10 @@ constexpr int kDspChunk = kDspConsumers * 32 * 16;   // x bytes per stage
 constexpr int kDspStageBytes = kDspChunk + 16;       // + the quad before the chunk
 constexpr int kDspStages = LLMOE_DSP_STAGES;
 constexpr int kDspThreads = 32 * (1 + kDspConsumers);
+#ifndef LLMOE_DSP_DEST_REGS
+#define LLMOE_DSP_DEST_REGS 8
+#endif
+constexpr int kDestRegs = LLMOE_DSP_DEST_REGS > 0 ? LLMOE_DSP_DEST_REGS : 1;  // destinations a dispatch thread keeps in registers
 
 __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const uint16_t* __restrict__ x,
                                                                const int64_t* __restrict__ idx) {
@@ -358,12 +382,13 @@ __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const
     if (sl >= 0) {
       const int dst = e / g.L, le = e % g.L;
       const uint64_t row = ((uint64_t)le * g.R + src) * g.T_max + sl;
-      d = reinterpret_cast<uintptr_t>(g.base + dst * g.rank_stride + g.recv_off + row * g.msg);
+      d = pack_dest(g.base + dst * g.rank_stride + g.recv_off + row * g.msg);
     }
     s_dst[q] = d;
   }
   __syncthreads();
   if (early) wait_prior_grid();  // the receive rows and signal words may be in use until now
+  clean_other_set(g);
   if (last) route_count_block(s, nblock);
 
   if (warp == 0) {
@@ -376,7 +401,10 @@ __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const
       st.issued = next;
     }
   } else {
-    const int ct = threadIdx.x - 32;  // 0 .. 127: the 16-byte quad of the chunk
+    const int ct = threadIdx.x - 32;  // the 16-byte quad of the chunk this thread moves
+    const bool small_k = LLMOE_DSP_DEST_REGS > 0 && g.K <= kDestRegs;
+    uintptr_t dreg[kDestRegs];  // top-k <= kDestRegs: the token's destinations, kept across its chunks
+    int cached_tl = -1;
     int it = 0;
     for (; it < n_iters; ++it) {
       const int sidx = it % kDspStages;
@@ -384,15 +412,26 @@ __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const
       const int tl = it / nch, c = it % nch;
       const int len = min(kDspChunk, row_bytes - c * kDspChunk);
       const uint8_t* sb = ring.stage(sidx);
+      const uintptr_t* dsts = s_dst + tl * g.K;
+      if (small_k && tl != cached_tl) {
+#pragma unroll
+        for (int k = 0; k < kDestRegs; ++k) dreg[k] = k < g.K ? dsts[k] : 0;
+        cached_tl = tl;
+      }
       if (ct * 16 < len) {
         const uint4 cur = *reinterpret_cast<const uint4*>(sb + 16 + 16 * ct);
         const uint4 prev = (c == 0 && ct == 0) ? make_uint4(0, 0, 0, (uint32_t)(t0 + tl))
                                                : *reinterpret_cast<const uint4*>(sb + 16 * ct);
         const int j = c * (kDspChunk / 16) + ct;
-        const uintptr_t* dsts = s_dst + tl * g.K;
-        for (int k = 0; k < g.K; ++k) {
-          const uintptr_t d = dsts[k];
-          if (d != 0) put_quad(reinterpret_cast<uint8_t*>(d), j, g.nq, prev, cur);
+        if (small_k) {
+#pragma unroll
+          for (int k = 0; k < kDestRegs; ++k)
+            if (dreg[k] != 0) put_quad(dreg[k], j, g.nq, prev, cur);
+        } else {
+          for (int k = 0; k < g.K; ++k) {
+            const uintptr_t d = dsts[k];
+            if (d != 0) put_quad(d, j, g.nq, prev, cur);
+          }
         }
       }
       __syncwarp();
@@ -475,6 +514,7 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
   }
   __syncthreads();
   if (early) wait_prior_grid();  // y and the signal words may come from the previous kernel
+  clean_other_set(g);
   if (last) route_count_block(s, nblock);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -625,6 +665,7 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   g->rank_stride = bs->rank_stride;
   g->recv_off = 2 * li.send + li.recv * (uint64_t)set;
   g->sig_off = 2 * li.send + 2 * li.recv + li.sig * (uint64_t)set;
+  g->other_sig_off = 2 * li.send + 2 * li.recv + li.sig * (uint64_t)(set ^ 1);
   g->msg = li.msg;
   g->err = bs->err;
   g->flags = bs->flags;

@@ -35,6 +35,7 @@ LLMOE_DEV_SLOT_RANGE = 4
 LLMOE_DEV_TIMEOUT = 5
 
 LLMOE_FLAG_INPUTS_READY = 1
+LLMOE_FLAG_CLEAN_OTHER_SET = 2
 
 LLMOE_MAX_TOPK = 32
 LLMOE_MAX_EXPERTS = 8192

@@ -80,6 +80,13 @@ typedef enum {
  * has completed.  Typical use: a combine whose topk_idx / topk_w came from a
  * router that ran before the expert kernels. */
 #define LLMOE_FLAG_INPUTS_READY 1u
+/* A dispatch or combine on set s also zeroes set s^1's num_experts signal
+ * words in every rank buffer (the llmoe_clean that the next call on set s^1
+ * needs), after the preceding kernel on the stream has completed.  A round
+ * then needs two launches: dispatch(set 0) and combine(set 1), each with this
+ * flag, after one llmoe_clean of set 0 before the first round.  Whatever
+ * reads the other set's words must do so before this call. */
+#define LLMOE_FLAG_CLEAN_OTHER_SET 2u
 
 /* Library limits (checked on the host). */
 #define LLMOE_MAX_TOPK 32

@@ -408,3 +408,28 @@ def test_inputs_ready_flag_in_cuda_graph_after_producer(L):
     d = r.check_dispatch()
     r.check_combine()
     r.check_canary(d)
+
+
+# ---------------------------------------------------------------------------
+# LLMOE_FLAG_CLEAN_OTHER_SET: two-launch rounds with the cleans fused
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["tiny", "skewed", "dsv3"])
+def test_fused_clean_rounds(L, name):
+    w = WORKLOADS[name]
+    r = Round(L, w, seed=14)
+    F = L.LLMOE_FLAG_CLEAN_OTHER_SET | L.LLMOE_FLAG_INPUTS_READY
+    bs_d = r.rb.buf_set(0, w.K, r.T_call, r.err, flags=F)
+    bs_c = r.rb.buf_set(1, w.K, r.T_call, r.err, flags=F)
+    r.rb.signal_words(1).fill_(CANARY_WORD)  # the first dispatch must clean set 1
+    L.llmoe_clean(r.rb.buf_set(0, w.K, r.T_call, r.err))
+    for rep in range(3):
+        L.llmoe_dispatch(r.x, r.idx, bs_d)
+        torch.cuda.synchronize()
+        assert not r.rb.signal_words(1).any(), "dispatch did not clean the other set"
+        r.check_dispatch()
+        L.llmoe_combine(r.y, r.idx, r.wt, r.out, bs_c)
+        torch.cuda.synchronize()
+        assert not r.rb.signal_words(0).any(), "combine did not clean the other set"
+        r.check_combine()
+        assert L.llmoe_get_error(bs_d) == 0  # no stale signal on any repeat
