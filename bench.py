@@ -310,7 +310,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     # another one so the written lines are evicted (and written back) before
     # the step's first event instead of inside the step
     flush_w = torch.empty(FLUSH_BYTES // 8, dtype=torch.int64, device="cuda")
-    flush_r = torch.ones(FLUSH_READ_BYTES // 4, dtype=torch.int32, device="cuda")
+    flush_r = torch.ones(FLUSH_READ_BYTES // 4, dtype=torch.float32, device="cuda")
 
     def flush():
         flush_w.zero_()
