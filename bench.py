@@ -116,6 +116,21 @@ def ncu_traffic(kernel: str, workload: str):
     return None
 
 
+def max_over_ranks(values, world: int):
+    """Elementwise maximum of a list of floats over all ranks (the slowest
+    rank's time); identity for one rank.  Uses the process group's device:
+    CUDA for nccl, CPU for gloo."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -385,18 +400,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     four_ms = [e[0].elapsed_time(e[1]) for e in ev4]
     disp_ms = [e[0].elapsed_time(e[1]) for e in evk]
     comb_ms = [e[1].elapsed_time(e[2]) for e in evk]
-    timed = torch.tensor([sum(step_ms), wall], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(timed, op=dist.ReduceOp.MAX)
-    round_us = float(timed[0]) / args.steps * 1e3
+    timed = max_over_ranks([sum(step_ms), wall], world)
+    round_us = timed[0] / args.steps * 1e3
 
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream)
-        if world > 1:
-            t = torch.tensor([e2e["value"]], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["value"] = float(t[0])
+        e2e["value"] = max_over_ranks([e2e["value"]], world)[0]
 
     if rank == 0:
         peak, peak_kind = measured_hbm_peak()
@@ -427,7 +437,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "dispatch_us": round(d_us, 3), "combine_us": round(c_us, 3),
             "round_us_four_calls": round(statistics.mean(four_ms) * 1e3, 3),
             "step_us_median": round(statistics.median(step_ms) * 1e3, 3),
-            "wall_s": round(float(timed[1]), 3),
+            "wall_s": round(timed[1], 3),
             "roofline": {"kernel": dom + "_kernel", "bound": "hbm", "achieved": round(dom_gbs, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                          "traffic": traffic, "algorithmic_bytes": algo[dom]},
