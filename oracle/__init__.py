@@ -17,6 +17,9 @@ function follows:
   values) and recv-count words.
 - ``combine``: the K-row gather, fp32 ``w * y`` in ascending k, bf16 store;
   LLMoEBuffer combine recv-flag words.
+- ``combine_staged``: the combine through the combine receive buffers
+  (LLMoEBuffer combine send / recv roles): messages [t | y row] at
+  combine_recv[e][t] of the source rank, then the reduction from them.
 - ``clean``: LLMoEBuffer::clean_meta.
 """
 from __future__ import annotations
@@ -99,6 +102,8 @@ def lib():
             L.oracle_dispatch.restype = i
             L.oracle_combine.argtypes = [i, i, i, i, i, i, P, P, P, P, P]
             L.oracle_combine.restype = i
+            L.oracle_combine_staged.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
+            L.oracle_combine_staged.restype = i
             L.oracle_clean.argtypes = [i, i, P]
             L.oracle_clean.restype = None
             _lib = L
@@ -231,6 +236,46 @@ def combine(y_rows, topk_idx: np.ndarray, topk_w: np.ndarray, hidden: int, num_e
     if rc != OK:
         raise OracleError(rc, "combine")
     return out, flag_words
+
+
+def _row_pointers(y_rows, hidden: int, nrows: int):
+    if isinstance(y_rows, tuple):
+        pool, row_map = y_rows
+        pool = np.ascontiguousarray(pool, dtype=np.uint16)
+        row_map = np.ascontiguousarray(row_map, dtype=np.int64)
+        assert pool.shape[1] == hidden and row_map.shape == (nrows,)
+        return (pool.ctypes.data + row_map * (2 * hidden)).astype(np.uint64), pool
+    dense = np.ascontiguousarray(y_rows, dtype=np.uint16)
+    assert dense.shape == (nrows, hidden)
+    return (dense.ctypes.data + np.arange(nrows, dtype=np.uint64) * np.uint64(2 * hidden)).astype(np.uint64), dense
+
+
+def combine_staged(y_rows, topk_idx: np.ndarray, topk_w: np.ndarray, hidden: int, num_experts: int,
+                   num_max_tokens: int | None = None):
+    """Expected staged combine: dict with msg_rank [n], msg_row [n] (row of
+    the source rank's combine receive region), msgs uint8 [n, 4 + 2H],
+    out uint16 [R, T, H], flag_words int64 [R, E]."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    R, T, K = idx.shape
+    T_max = T if num_max_tokens is None else num_max_tokens
+    ptrs, keep = _row_pointers(y_rows, hidden, num_experts * R * T_max)
+    cap = max(R * T * K, 1)
+    msg_rank = np.empty(cap, dtype=np.int64)
+    msg_row = np.empty(cap, dtype=np.int64)
+    msgs = np.empty((cap, 4 + 2 * hidden), dtype=np.uint8)
+    out = np.empty((R, T, hidden), dtype=np.uint16)
+    flag_words = np.empty((R, num_experts), dtype=np.int64)
+    n = ctypes.c_int64(0)
+    rc = lib().oracle_combine_staged(R, T_max, T, hidden, num_experts, K, _ptr(ptrs), _ptr(idx), _ptr(w),
+                                     _ptr(msg_rank), _ptr(msg_row), _ptr(msgs), _ptr(out), _ptr(flag_words),
+                                     ctypes.addressof(n))
+    del keep
+    if rc != OK:
+        raise OracleError(rc, "combine_staged")
+    n = n.value
+    return {"msg_rank": msg_rank[:n], "msg_row": msg_row[:n], "msgs": msgs[:n], "out": out,
+            "flag_words": flag_words, "n": n}
 
 
 def clean(num_ranks: int, num_experts: int) -> np.ndarray:

@@ -364,3 +364,86 @@ int oracle_combine(int R, int T_max, int T, int H, int E, int K, const uint16_t*
 void oracle_clean(int R, int E, int64_t* sig_words) {
   for (int64_t i = 0; i < (int64_t)R * E; ++i) sig_words[i] = 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Staged combine (LLMoEBuffer combine send / recv roles)                   */
+/* ------------------------------------------------------------------------ */
+
+/* The combine routed through the combine receive buffers.  Step one: every
+ * unmasked entry (src, t, k) choosing expert e has its expert output row
+ * returned to rank src as one message [int32 t][y_row as bf16] at row
+ * e * T_max + t of rank src's combine receive region (combine_recv[e][t]: the
+ * num_experts * num_tokens messages the layout sizes that buffer for).
+ * Step two: rank src reduces out[src][t] from the payloads of its messages
+ * combine_recv[e_k][t], over ascending k, with the arithmetic of
+ * oracle_combine.  Flag word e of rank src = rows expert e returned to src.
+ *
+ * Outputs: msg_rank[n], msg_row[n], msgs[n][4 + 2H] in (src, t, k) order of
+ * the unmasked entries, out[R][T][H], flag_words[R][E].  *n_out = n. */
+int oracle_combine_staged(int R, int T_max, int T, int H, int E, int K, const uint16_t* const* y_rows,
+                          const int64_t* idx, const float* w, int64_t* msg_rank, int64_t* msg_row, uint8_t* msgs,
+                          uint16_t* out, int64_t* flag_words, int64_t* n_out) {
+  *n_out = 0;
+  if (R < 1 || T_max < 1 || T < 0 || T > T_max || H < 1 || E < 1 || K < 1 || E % R != 0) return ORACLE_BAD_ARG;
+  int64_t ntk = (int64_t)R * T * K;
+  int32_t* slot = (int32_t*)malloc((size_t)(ntk > 0 ? ntk : 1) * sizeof(int32_t));
+  int64_t* cnt = (int64_t*)malloc((size_t)E * R * sizeof(int64_t));
+  int64_t* where = (int64_t*)malloc((size_t)(ntk > 0 ? ntk : 1) * sizeof(int64_t));
+  float* acc = (float*)malloc((size_t)H * sizeof(float));
+  if (!slot || !cnt || !where || !acc) {
+    free(slot); free(cnt); free(where); free(acc);
+    return ORACLE_BAD_ARG;
+  }
+  int rc = oracle_route(R, T, K, E, idx, slot, cnt);
+  if (rc != ORACLE_OK) {
+    free(slot); free(cnt); free(where); free(acc);
+    return rc;
+  }
+  const size_t msg = 4 + 2 * (size_t)H;
+  /* step one: the returned messages */
+  int64_t n = 0;
+  for (int src = 0; src < R; ++src) {
+    for (int t = 0; t < T; ++t) {
+      for (int k = 0; k < K; ++k) {
+        int64_t pos = ((int64_t)src * T + t) * K + k;
+        int64_t e = idx[pos];
+        where[pos] = -1;
+        if (e < 0) continue;
+        int64_t yrow = e * R * T_max + (int64_t)src * T_max + slot[pos];
+        msg_rank[n] = src;
+        msg_row[n] = e * T_max + t;
+        uint8_t* m = msgs + (size_t)n * msg;
+        int32_t header = t;
+        memcpy(m, &header, 4);
+        memcpy(m + 4, y_rows[yrow], 2 * (size_t)H);
+        where[pos] = n;
+        n += 1;
+      }
+    }
+  }
+  /* step two: each source rank reduces from its received messages */
+  for (int src = 0; src < R; ++src) {
+    for (int t = 0; t < T; ++t) {
+      for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        int64_t pos = ((int64_t)src * T + t) * K + k;
+        if (where[pos] < 0) continue;
+        const uint8_t* payload = msgs + (size_t)where[pos] * msg + 4;
+        float wk = w[pos];
+        for (int h = 0; h < H; ++h) {
+          uint16_t b;
+          memcpy(&b, payload + 2 * (size_t)h, 2);
+          float p = wk * oracle_bf16_to_f32(b);
+          acc[h] = acc[h] + p;
+        }
+      }
+      uint16_t* o = out + ((size_t)src * T + t) * H;
+      for (int h = 0; h < H; ++h) o[h] = oracle_f32_to_bf16(acc[h]);
+    }
+  }
+  for (int src = 0; src < R; ++src)
+    for (int e = 0; e < E; ++e) flag_words[(int64_t)src * E + e] = cnt[(int64_t)e * R + src];
+  *n_out = n;
+  free(slot); free(cnt); free(where); free(acc);
+  return ORACLE_OK;
+}
