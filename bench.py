@@ -339,6 +339,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dispatch_plain = llmoe.bind_dispatch(x, idx, bs0_plain, stream)
     combine_plain = llmoe.bind_combine(y, idx, wt, out, bs1_plain, stream)
 
+    combine_staged = llmoe.Bound("llmoe_combine_staged", combine.args, combine.keep)
+
     def step():
         dispatch()
         combine()
@@ -364,6 +366,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         return [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
 
     ev, ev4, evk = new_events(args.steps, 2), new_events(args.steps, 2), new_events(args.steps, 3)
+    evs = new_events(args.steps, 2)
     with ClockSampler(gpu_id_for(local_rank)) as clocks:
         torch.cuda.synchronize()
         if world > 1:
@@ -395,7 +398,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             e[1].record(stream)
             combine()
             e[2].record(stream)
+        # the staged combine (messages through combine_recv[e][t], then the reduction)
+        for e in evs:
+            flush()
+            dispatch()
+            e[0].record(stream)
+            combine_staged()
+            e[1].record(stream)
         torch.cuda.synchronize()
+    staged_ms = [e[0].elapsed_time(e[1]) for e in evs]
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     four_ms = [e[0].elapsed_time(e[1]) for e in ev4]
     disp_ms = [e[0].elapsed_time(e[1]) for e in evk]
@@ -436,6 +447,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "algorithmic_bytes_per_round": algo["round"],
             "dispatch_us": round(d_us, 3), "combine_us": round(c_us, 3),
             "round_us_four_calls": round(statistics.mean(four_ms) * 1e3, 3),
+            "staged_combine_us": round(statistics.mean(staged_ms) * 1e3, 3),
+            "staged_combine_gbs": round((algo["combine"] + 2 * n_valid * (4 + 2 * w.H)) /
+                                        (statistics.mean(staged_ms) * 1e3) / 1e3, 1),
             "step_us_median": round(statistics.median(step_ms) * 1e3, 3),
             "wall_s": round(timed[1], 3),
             "roofline": {"kernel": dom + "_kernel", "bound": "hbm", "achieved": round(dom_gbs, 1),

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <climits>
 
 #include "llmoe.h"
@@ -559,6 +560,145 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
   }
 }
 
+// ---------------------------------------------------------------------------
+// staged combine: put the expert output rows as messages into the source
+// ranks' combine receive regions, then reduce from them
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 shfl_up16(const uint4& v) {
+  return make_uint4(__shfl_up_sync(0xffffffffu, v.x, 1), __shfl_up_sync(0xffffffffu, v.y, 1),
+                    __shfl_up_sync(0xffffffffu, v.z, 1), __shfl_up_sync(0xffffffffu, v.w, 1));
+}
+__device__ __forceinline__ uint4 shfl_down16(const uint4& v) {
+  return make_uint4(__shfl_down_sync(0xffffffffu, v.x, 1), __shfl_down_sync(0xffffffffu, v.y, 1),
+                    __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
+}
+
+// Payload quad from two consecutive aligned quads a, b when the payload starts
+// `phase` words into a: words phase .. phase+3 of (a, b).
+__device__ __forceinline__ uint4 unshift_words(const uint4& a, const uint4& b, int phase) {
+  switch (phase) {
+    case 0: return a;
+    case 1: return make_uint4(a.y, a.z, a.w, b.x);
+    case 2: return make_uint4(a.z, a.w, b.x, b.y);
+    default: return make_uint4(a.w, b.x, b.y, b.z);
+  }
+}
+
+// Put: entry (src, t, k) choosing expert e sends [t][y row] to rank src's
+// combine_recv[e][t] (row e * T_max + t of its receive region).  One warp
+// moves 32 quads of one entry's row per unit; rank src's flag words are
+// written by the CTA of its last token block.
+__global__ void __launch_bounds__(kThreads) combine_put_kernel(Geometry g, const uint16_t* __restrict__ y,
+                                                               const int64_t* __restrict__ idx) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const RouteSmem s = carve_route(smem, g);
+  const int TBK = g.TB * g.K;
+  const uint4** s_src = reinterpret_cast<const uint4**>(s.slot + TBK + (g.E & 1));
+  uintptr_t* s_dst = reinterpret_cast<uintptr_t*>(s_src + TBK);
+
+  const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
+  const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
+  const bool last = (b == g.nblk - 1);
+  const int nblock = (t1 - t0) * g.K;
+  const bool early = (g.flags & LLMOE_FLAG_INPUTS_READY) != 0;
+  release_next_grid();
+  if (!early) wait_prior_grid();
+
+  route_hist(g, idx, src, t0, t1, s);
+  uint8_t* rbase = g.base + src * g.rank_stride + g.recv_off;
+  for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
+    const int e = s.ent[q], sl = route_slot(g, s, q);
+    const uint4* row = nullptr;
+    uintptr_t d = 0;
+    if (sl >= 0) {
+      row = reinterpret_cast<const uint4*>(y + ((uint64_t)e * g.R * g.T_max + (uint64_t)src * g.T_max + sl) * g.H);
+      d = pack_dest(rbase + ((uint64_t)e * g.T_max + (t0 + q / g.K)) * g.msg);
+    }
+    s_src[q] = row;
+    s_dst[q] = d;
+  }
+  __syncthreads();
+  if (early) wait_prior_grid();
+  clean_other_set(g);
+  if (last) route_count_block(s, nblock);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nunits = nblock * g.nchunks;
+  for (int u = warp; u < nunits; u += kThreads / 32) {
+    const int q = u / g.nchunks, c = u % g.nchunks;
+    const uint4* row = s_src[q];
+    if (row == nullptr) continue;  // the whole warp: masked entry
+    const int t = t0 + q / g.K, j = c * 32 + lane;
+    const uint4 cur = j < g.nq ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
+    uint4 prev = shfl_up16(cur);
+    if (lane == 0) prev = j == 0 ? make_uint4(0, 0, 0, (uint32_t)t) : __ldg(row + j - 1);
+    if (j < g.nq) put_quad(s_dst[q], j, g.nq, prev, cur);
+  }
+
+  if (last) {
+    __syncthreads();
+    // rank src's word e = rows expert e returned to src
+    int64_t* w = reinterpret_cast<int64_t*>(g.base + src * g.rank_stride + g.sig_off);
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) put_signal(g, w + e, s.hist[e]);
+  }
+}
+
+// Reduce: out[src][t] from the payloads of combine_recv[e_k][t], ascending k.
+// One warp per (token, 32-quad chunk); the messages sit at 4-byte phases, so
+// each lane loads its aligned quad, takes the next one from its neighbour and
+// shifts the payload words into place.
+__global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, const int64_t* __restrict__ idx,
+                                                                  const float* __restrict__ topk_w,
+                                                                  uint16_t* __restrict__ out) {
+  release_next_grid();
+  wait_prior_grid();
+  const int lane = threadIdx.x & 31;
+  const int64_t nunits = (int64_t)g.R * g.T * g.nchunks;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < nunits; u += nwarps) {
+    const int c = (int)(u % g.nchunks);
+    const int64_t tok = u / g.nchunks;
+    const int src = (int)(tok / g.T), t = (int)(tok % g.T);
+    long long e_lane = -1;
+    float w_lane = 0.0f;
+    if (lane < g.K) {
+      e_lane = idx[tok * g.K + lane];
+      w_lane = topk_w[tok * g.K + lane];
+    }
+    const int j = c * 32 + lane;
+    const uint8_t* rbase = g.base + src * g.rank_stride + g.recv_off;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int k = 0; k < g.K; ++k) {  // ascending k
+      const long long e = __shfl_sync(0xffffffffu, e_lane, k);
+      const float wk = __shfl_sync(0xffffffffu, w_lane, k);
+      if (e < 0 || e >= g.E) continue;  // the whole warp
+      const uint8_t* msg = rbase + ((uint64_t)e * g.T_max + t) * g.msg;
+      const uintptr_t pa = reinterpret_cast<uintptr_t>(msg) + 4;
+      const int phase = (int)((pa >> 2) & 3);
+      const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
+      // lane j holds aligned quad j; the quad past the payload end feeds the
+      // last lane when the payload is not aligned
+      uint4 a = make_uint4(0, 0, 0, 0);
+      if (j < g.nq || (j == g.nq && phase != 0)) a = __ldg(qb + j);
+      uint4 b = shfl_down16(a);
+      if (lane == 31 && phase != 0 && j < g.nq) b = __ldg(qb + j + 1);
+      if (g.err != nullptr && j == 0 && *reinterpret_cast<const int32_t*>(msg) != t)
+        report(g.err, LLMOE_DEV_BAD_MESSAGE);
+      if (j < g.nq) axpy_quad(acc, wk, unshift_words(a, b, phase));
+    }
+    if (j < g.nq) {
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      reinterpret_cast<uint4*>(out + ((int64_t)src * g.T + t) * g.H)[j] = o;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) route_kernel(Geometry g, const int64_t* __restrict__ idx,
                                                          int32_t* __restrict__ slot_out,
                                                          int64_t* __restrict__ counts) {
@@ -695,7 +835,7 @@ void set_blocking(Geometry* g, int blocks_per_sm) {
   g->nblk = g->T > 0 ? (g->T + g->TB - 1) / g->TB : 1;
 }
 
-int g_smem_optin[64][3] = {{0}};
+int g_smem_optin[64][8] = {{0}};
 
 // Opts a kernel in to more than 48 KB of dynamic shared memory (once per
 // device and size).
@@ -712,7 +852,14 @@ int set_smem(int id, const void* fn, size_t bytes) {
   return LLMOE_SUCCESS;
 }
 
-enum KernelId { kRouteKernel = 0, kDispatchKernel = 1, kCombineKernel = 2, kNumKernels = 3 };
+enum KernelId {
+  kRouteKernel = 0,
+  kDispatchKernel = 1,
+  kCombineKernel = 2,
+  kCombinePutKernel = 3,
+  kCombineReduceKernel = 4,
+  kNumKernels = 5
+};
 int g_occupancy[64][kNumKernels] = {{0}};
 
 // Resident CTAs per SM of a kernel at kThreads threads and `smem` bytes,
@@ -830,6 +977,36 @@ int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const float* topk_
   const size_t smem = combine_smem_bytes(g);
   if ((rc = set_smem(kCombineKernel, (const void*)combine_kernel, smem)) != LLMOE_SUCCESS) return rc;
   return launch(combine_kernel, g.R * g.nblk, kCmbThreads, smem, stream, g, y, topk_idx, topk_w, out);
+}
+
+int llmoe_combine_staged(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
+                         const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
+  Geometry g;
+  int rc = make_geometry(bs, true, &g);
+  if (rc != LLMOE_SUCCESS) return rc;
+  if (g.T > 0 && (y == nullptr || topk_idx == nullptr || topk_w == nullptr || out == nullptr || !aligned(y, 16) ||
+                  !aligned(out, 16) || !aligned(topk_idx, 8) || !aligned(topk_w, 4)))
+    return LLMOE_ERR_INVALID_ARGUMENT;
+  if (g.T > 0) {
+    const uintptr_t yb = reinterpret_cast<uintptr_t>(y), ob = reinterpret_cast<uintptr_t>(out);
+    const uintptr_t ye = yb + (uintptr_t)g.E * g.R * g.T_max * g.H * 2, oe = ob + (uintptr_t)g.R * g.T * g.H * 2;
+    if (ob < ye && yb < oe) return LLMOE_ERR_INVALID_ARGUMENT;
+  }
+  const size_t put_extra = (sizeof(void*) + sizeof(uintptr_t)) * (size_t)g.K;
+  set_blocking(&g, blocks_per_sm(kCombinePutKernel, (const void*)combine_put_kernel, kThreads,
+                                 route_smem_bytes(g) + put_extra));
+  const size_t smem = route_smem_bytes(g) + (sizeof(void*) + sizeof(uintptr_t)) * (size_t)g.TB * g.K;
+  if ((rc = set_smem(kCombinePutKernel, (const void*)combine_put_kernel, smem)) != LLMOE_SUCCESS) return rc;
+  if ((rc = launch(combine_put_kernel, g.R * g.nblk, kThreads, smem, stream, g, y, topk_idx)) != LLMOE_SUCCESS)
+    return rc;
+  if (g.T == 0) return LLMOE_SUCCESS;
+  const int64_t warps = (int64_t)g.R * g.T * g.nchunks;
+  const int64_t wave = (int64_t)num_sms() * blocks_per_sm(kCombineReduceKernel, (const void*)combine_reduce_kernel,
+                                                          kThreads, 0);
+  const int64_t blocks = std::min<int64_t>(wave, (warps + kThreads / 32 - 1) / (kThreads / 32));
+  Geometry gr = g;
+  gr.flags &= ~LLMOE_FLAG_CLEAN_OTHER_SET;  // the put kernel already cleaned
+  return launch(combine_reduce_kernel, (unsigned)blocks, kThreads, 0, stream, gr, topk_idx, topk_w, out);
 }
 
 int llmoe_clean(const llmoe_buf_set_t* bs, llmoe_stream_t stream) {

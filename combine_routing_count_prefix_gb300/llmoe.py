@@ -33,6 +33,7 @@ LLMOE_DEV_DUPLICATE = 2
 LLMOE_DEV_STALE_SIGNAL = 3
 LLMOE_DEV_SLOT_RANGE = 4
 LLMOE_DEV_TIMEOUT = 5
+LLMOE_DEV_BAD_MESSAGE = 6
 
 LLMOE_FLAG_INPUTS_READY = 1
 LLMOE_FLAG_CLEAN_OTHER_SET = 2
@@ -41,7 +42,7 @@ LLMOE_MAX_TOPK = 32
 LLMOE_MAX_EXPERTS = 8192
 
 EXPORTS = ("llmoe_layout_bytes", "llmoe_layout_offsets", "llmoe_route", "llmoe_dispatch", "llmoe_combine",
-           "llmoe_clean", "llmoe_get_error", "llmoe_status_string")
+           "llmoe_combine_staged", "llmoe_clean", "llmoe_get_error", "llmoe_status_string")
 
 
 class llmoe_buf_set_t(ctypes.Structure):
@@ -73,6 +74,8 @@ _lib.llmoe_dispatch.argtypes = [_P, _P, _BS, _P]
 _lib.llmoe_dispatch.restype = _I
 _lib.llmoe_combine.argtypes = [_P, _P, _P, _P, _BS, _P]
 _lib.llmoe_combine.restype = _I
+_lib.llmoe_combine_staged.argtypes = [_P, _P, _P, _P, _BS, _P]
+_lib.llmoe_combine_staged.restype = _I
 _lib.llmoe_clean.argtypes = [_BS, _P]
 _lib.llmoe_clean.restype = _I
 _lib.llmoe_get_error.argtypes = [_BS, _P, ctypes.POINTER(ctypes.c_int32), _I]
@@ -153,6 +156,11 @@ def llmoe_dispatch(x, topk_idx, bs: llmoe_buf_set_t, stream=None) -> None:
 def llmoe_combine(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=None) -> None:
     _check(_lib.llmoe_combine(_addr(y, "bf16"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"), _addr(out, "bf16"),
                               ctypes.byref(bs), _stream(stream)), "llmoe_combine")
+
+
+def llmoe_combine_staged(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=None) -> None:
+    _check(_lib.llmoe_combine_staged(_addr(y, "bf16"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"),
+                                     _addr(out, "bf16"), ctypes.byref(bs), _stream(stream)), "llmoe_combine_staged")
 
 
 def llmoe_clean(bs: llmoe_buf_set_t, stream=None) -> None:

@@ -70,6 +70,7 @@ typedef enum {
 #define LLMOE_DEV_STALE_SIGNAL 3 /* a signal word was non-zero on entry (a clean was skipped) */
 #define LLMOE_DEV_SLOT_RANGE 4   /* a bucket overflowed num_max_tokens (only reachable with duplicates) */
 #define LLMOE_DEV_TIMEOUT 5      /* a bounded wait inside a kernel expired (a copy never completed) */
+#define LLMOE_DEV_BAD_MESSAGE 6  /* a staged-combine message header does not name its token */
 
 /* llmoe_buf_set_t.flags */
 /* The call's read-only routing inputs (topk_idx and topk_w, and x for a
@@ -184,6 +185,23 @@ LLMOE_API int llmoe_dispatch(const uint16_t* x, const int64_t* topk_idx, const l
  * set-`set` signal word e = number of rows expert e returned to src. */
 LLMOE_API int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
                   const llmoe_buf_set_t* bs, llmoe_stream_t stream);
+
+/* Staged combine (LLMoEBuffer combine receive buffer and recv-flag words): the
+ * same inputs and result as llmoe_combine, routed through the layout's
+ * combine buffers as the expert-parallel exchange would route it.  First, for
+ * every unmasked entry (src, t, k) choosing expert e, the expert output row
+ * returns to rank src as the message [int32 t][y row] at row e * T + t of
+ * rank src's set-`set` receive region (combine_recv[e][t]: the
+ * num_experts * num_tokens messages of the combine receive buffer), and rank
+ * src's flag word e is set to the rows e returned.  Then rank src reduces
+ * out[src][t] from those messages' payloads exactly as llmoe_combine does
+ * (ascending k, fp32 products then sums, bf16 round-to-nearest-even).  Two
+ * kernels; the second starts after the first has completed.  Validate mode
+ * also checks each message header (LLMOE_DEV_BAD_MESSAGE).  The set's receive
+ * region is overwritten at those rows: it aliases the dispatch receive region
+ * of the same set. */
+LLMOE_API int llmoe_combine_staged(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
+                                   const llmoe_buf_set_t* bs, llmoe_stream_t stream);
 
 /* Clean (LLMoEBuffer::clean_meta): zero the num_experts int64 signal words
  * of buffer set `set` in each of the R rank buffers.  This resets both the

@@ -433,3 +433,63 @@ def test_fused_clean_rounds(L, name):
         assert not r.rb.signal_words(0).any(), "combine did not clean the other set"
         r.check_combine()
         assert L.llmoe_get_error(bs_d) == 0  # no stale signal on any repeat
+
+
+# ---------------------------------------------------------------------------
+# staged combine: messages through combine_recv[e][t], then the reduction
+# ---------------------------------------------------------------------------
+
+def run_staged(L, r: Round):
+    L.llmoe_clean(r.bs_c)
+    L.llmoe_combine_staged(r.y, r.idx, r.wt, r.out, r.bs_c)
+    torch.cuda.synchronize()
+    assert L.llmoe_get_error(r.bs_c) == 0
+    w, inp = r.w, r.inp
+    st = oracle.combine_staged((inp["y_pool"], inp["y_row_map"]), inp["topk_idx"], inp["topk_w"], w.H, w.E,
+                               num_max_tokens=w.T)
+    recv = r.rb.recv_rows(r.cs)
+    if st["n"]:
+        got = recv[dev(st["msg_rank"]), dev(st["msg_row"])].cpu().numpy()
+        bad = np.nonzero((got != st["msgs"]).any(axis=1))[0]
+        assert bad.size == 0, f"{bad.size} of {st['n']} staged messages differ"
+    out = r.out.cpu().numpy().view(np.uint16)
+    dist = np.abs(ordinal(out) - ordinal(st["out"]))
+    assert dist.max(initial=0) <= 1 and int((dist != 0).sum()) == 0
+    assert np.array_equal(r.rb.signal_words(r.cs).cpu().numpy(), st["flag_words"])
+    # nothing but those messages and the signal words was written
+    if st["n"]:
+        recv[dev(st["msg_rank"]), dev(st["msg_row"])] = CANARY
+    r.rb.signal_words(0).fill_(CANARY_WORD)
+    r.rb.signal_words(1).fill_(CANARY_WORD)
+    assert all_equal_chunked(r.rb.storage, CANARY)
+    return st
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "many_small", "large"])
+def test_staged_combine(L, name):
+    run_staged(L, Round(L, WORKLOADS[name], seed=31))
+
+
+@pytest.mark.parametrize("R,E,K,H,T", [(1, 8, 2, 8, 3), (3, 15, 8, 56, 37), (32, 32, 1, 264, 3), (2, 8, 8, 264, 1),
+                                       (8, 64, 6, 4096, 9)])
+def test_staged_combine_shapes(L, R, E, K, H, T):
+    w = Workload("staged", R, T, H, E, K, mask_p=0.3 if K > 1 else 0.0)
+    run_staged(L, Round(L, w, seed=R + E + K + H + T))
+
+
+def test_staged_combine_fewer_tokens_and_set_one(L):
+    w = WORKLOADS["dsv3"].with_(H=1024)
+    run_staged(L, Round(L, w, seed=33, tokens=77, dispatch_set=1))
+
+
+def test_staged_equals_direct_on_gpu(L):
+    w = WORKLOADS["skewed"]
+    r = Round(L, w, seed=34)
+    L.llmoe_clean(r.bs_c)
+    L.llmoe_combine(r.y, r.idx, r.wt, r.out, r.bs_c)
+    direct = r.out.clone()
+    r.out.fill_(OUT_CANARY)
+    L.llmoe_clean(r.bs_c)
+    L.llmoe_combine_staged(r.y, r.idx, r.wt, r.out, r.bs_c)
+    torch.cuda.synchronize()
+    assert torch.equal(direct, r.out)
