@@ -7,9 +7,9 @@ path and the CPU oracle can both be fed from it without sharing any of the
 method.
 
 All draws come from one CPU ``torch.Generator`` seeded per call, in a fixed
-order: x, routing, weights, mask, expert-output pool.  bf16 values are fp32
-draws cast by PyTorch (round to nearest even) and are handed out as their
-uint16 bit patterns.
+order: x, routing, weights, mask, expert-output pool.  Payload values are
+fp32 draws in the payload type: bf16 and fp16 cast by PyTorch (round to
+nearest even) and handed out as their uint16 bit patterns, fp32 as is.
 
 Workloads (tokens per rank T, hidden H, experts E over R simulated ranks,
 top-k K):
@@ -86,6 +86,18 @@ def _bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+def _payload(t: torch.Tensor, dtype: str) -> np.ndarray:
+    """fp32 draws as the payload type: bf16 / fp16 bit patterns (uint16, cast
+    by PyTorch with round to nearest even) or fp32 values."""
+    if dtype == "bf16":
+        return _bf16_bits(t)
+    if dtype == "fp16":
+        return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    if dtype == "fp32":
+        return t.numpy().astype(np.float32)
+    raise ValueError(dtype)
+
+
 def splitmix64(v: np.ndarray) -> np.ndarray:
     """SplitMix64 output function (Steele, Lea, Flood 2014) on uint64 words."""
     z = v.astype(np.uint64) + np.uint64(0x9E3779B97F4A7C15)
@@ -94,14 +106,17 @@ def splitmix64(v: np.ndarray) -> np.ndarray:
     return z ^ (z >> np.uint64(31))
 
 
-def make_inputs(w: Workload, seed: int = 0, tokens: int | None = None, pool_rows: int = POOL_ROWS) -> dict:
+def make_inputs(w: Workload, seed: int = 0, tokens: int | None = None, pool_rows: int = POOL_ROWS,
+                dtype: str = "bf16") -> dict:
     """Draw one round's inputs.
 
     tokens: tokens per rank in this call (default T); the layout and the
     expert-output matrix stay sized for T.
-    Returns numpy arrays: x uint16 [R, tokens, H], topk_idx int64
-    [R, tokens, K] (-1 = masked), topk_w float32 [R, tokens, K],
-    y_pool uint16 [P, H], y_row_map int64 [E * R * T].
+    dtype: payload type of x and y ("bf16", "fp16" as uint16 bit patterns,
+    "fp32" as float32).
+    Returns numpy arrays: x [R, tokens, H], topk_idx int64 [R, tokens, K]
+    (-1 = masked), topk_w float32 [R, tokens, K], y_pool [P, H],
+    y_row_map int64 [E * R * T].
     """
     n_tok = w.T if tokens is None else tokens
     assert 0 <= n_tok <= w.T and w.E % w.R == 0 and 1 <= w.K <= w.E
@@ -114,7 +129,7 @@ def make_inputs(w: Workload, seed: int = 0, tokens: int | None = None, pool_rows
         xf = torch.randn(rows * H, generator=g, dtype=torch.float32)
     else:
         xf = torch.rand(rows * H, generator=g, dtype=torch.float32) * 2.0 - 1.0
-    x = _bf16_bits(xf).reshape(R, n_tok, H)
+    x = _payload(xf, dtype).reshape(R, n_tok, H)
     del xf
 
     # routing: K distinct experts per token
@@ -139,7 +154,7 @@ def make_inputs(w: Workload, seed: int = 0, tokens: int | None = None, pool_rows
     # expert-output pool and row map
     nrows = E * R * w.T
     P = min(nrows, pool_rows)
-    pool = _bf16_bits(torch.randn(P * H, generator=g, dtype=torch.float32)).reshape(P, H)
+    pool = _payload(torch.randn(P * H, generator=g, dtype=torch.float32), dtype).reshape(P, H)
     if nrows <= pool_rows:
         row_map = np.arange(nrows, dtype=np.int64)
     else:

@@ -39,6 +39,9 @@ _LOCK = threading.Lock()
 _lib = None
 
 OK, BAD_EXPERT, DUPLICATE = 0, 1, 2
+
+# payload element types of LLMoEBufferLayout<T>: (code, bytes, numpy dtype of the stored values)
+DTYPES = {"bf16": (0, 2, np.uint16), "fp16": (1, 2, np.uint16), "fp32": (2, 4, np.float32)}
 BAD_ARG, ASSERT, OVERFLOW = -1, -2, -3
 
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-Wall", "-Wextra"]
@@ -49,7 +52,7 @@ def build(force: bool = False) -> str:
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + f".{os.getpid()}.tmp"
-        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC], check=True)
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
         os.replace(tmp, _SO)
     return _SO
 
@@ -92,17 +95,23 @@ def lib():
             L.oracle_f32_to_bf16.restype = ctypes.c_uint16
             L.oracle_f32_to_bf16_array.argtypes = [P, P, ctypes.c_int64]
             L.oracle_f32_to_bf16_array.restype = None
+            L.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+            L.oracle_f16_to_f32.restype = ctypes.c_float
+            L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+            L.oracle_f32_to_f16.restype = ctypes.c_uint16
+            L.oracle_f32_to_f16_array.argtypes = [P, P, ctypes.c_int64]
+            L.oracle_f32_to_f16_array.restype = None
             L.oracle_layout.argtypes = [i, i, i, i, i, ctypes.POINTER(Layout)]
             L.oracle_layout.restype = i
             L.oracle_size_hint.argtypes = [i, i, i, i, i]
             L.oracle_size_hint.restype = ctypes.c_uint64
             L.oracle_route.argtypes = [i, i, i, i, P, P, P]
             L.oracle_route.restype = i
-            L.oracle_dispatch.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P]
+            L.oracle_dispatch.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, P]
             L.oracle_dispatch.restype = i
-            L.oracle_combine.argtypes = [i, i, i, i, i, i, P, P, P, P, P]
+            L.oracle_combine.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P]
             L.oracle_combine.restype = i
-            L.oracle_combine_staged.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
+            L.oracle_combine_staged.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
             L.oracle_combine_staged.restype = i
             L.oracle_clean.argtypes = [i, i, P]
             L.oracle_clean.restype = None
@@ -131,6 +140,21 @@ def bf16_to_f32(b: int) -> float:
 
 def f32_to_bf16(f: float) -> int:
     return int(lib().oracle_f32_to_bf16(float(np.float32(f))))
+
+
+def f16_to_f32(h: int) -> float:
+    return float(lib().oracle_f16_to_f32(int(h)))
+
+
+def f32_to_f16(f: float) -> int:
+    return int(lib().oracle_f32_to_f16(float(np.float32(f))))
+
+
+def f32_to_f16_array(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint16)
+    lib().oracle_f32_to_f16_array(_ptr(a), _ptr(out), a.size)
+    return out
 
 
 def f32_to_bf16_array(a: np.ndarray) -> np.ndarray:
@@ -172,15 +196,18 @@ def route(topk_idx: np.ndarray, num_experts: int):
     return slot, cnt
 
 
-def dispatch(x: np.ndarray, topk_idx: np.ndarray, num_experts: int, num_max_tokens: int | None = None):
+def dispatch(x: np.ndarray, topk_idx: np.ndarray, num_experts: int, num_max_tokens: int | None = None,
+             dtype: str = "bf16"):
     """Expected dispatch result, compact.
 
-    x: uint16 bf16 bit patterns [R, T, H]; topk_idx: int64 [R, T, K].
-    Returns dict with row_rank [n], row_index [n], msgs uint8 [n, 4 + 2H]
+    x: [R, T, H] payload values (uint16 bit patterns for bf16 / fp16,
+    float32 for fp32); topk_idx: int64 [R, T, K].
+    Returns dict with row_rank [n], row_index [n], msgs uint8 [n, 4 + H*size]
     (in (src, t, k) order over unmasked entries) and count_words int64 [R, E]
     (rank r's E recv-count words).
     """
-    x = np.ascontiguousarray(x, dtype=np.uint16)
+    code, es, npdt = DTYPES[dtype]
+    x = np.ascontiguousarray(x, dtype=npdt)
     idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
     R, T, H = x.shape
     K = idx.shape[2]
@@ -189,10 +216,10 @@ def dispatch(x: np.ndarray, topk_idx: np.ndarray, num_experts: int, num_max_toke
     cap = max(R * T * K, 1)
     row_rank = np.empty(cap, dtype=np.int64)
     row_index = np.empty(cap, dtype=np.int64)
-    msgs = np.empty((cap, 4 + 2 * H), dtype=np.uint8)
+    msgs = np.empty((cap, 4 + es * H), dtype=np.uint8)
     count_words = np.empty((R, num_experts), dtype=np.int64)
     n = ctypes.c_int64(0)
-    rc = lib().oracle_dispatch(R, T_max, T, H, num_experts, K, _ptr(x), _ptr(idx), _ptr(row_rank),
+    rc = lib().oracle_dispatch(R, T_max, T, H, num_experts, K, code, _ptr(x), _ptr(idx), _ptr(row_rank),
                                _ptr(row_index), _ptr(msgs), _ptr(count_words), ctypes.addressof(n))
     if rc != OK:
         raise OracleError(rc, "dispatch")
@@ -202,35 +229,24 @@ def dispatch(x: np.ndarray, topk_idx: np.ndarray, num_experts: int, num_max_toke
 
 
 def combine(y_rows, topk_idx: np.ndarray, topk_w: np.ndarray, hidden: int, num_experts: int,
-            num_max_tokens: int | None = None):
+            num_max_tokens: int | None = None, dtype: str = "bf16"):
     """Expected combine result.
 
-    y_rows: either a uint16 array [E * R * T_max, H] (dense expert outputs in
-    receive-row order) or a pair (pool uint16 [P, H], row_map int64
-    [E * R * T_max]) meaning row r is pool[row_map[r]].
-    Returns (out uint16 [R, T, H], flag_words int64 [R, E]).
+    y_rows: either an array [E * R * T_max, H] (dense expert outputs in
+    receive-row order) or a pair (pool [P, H], row_map int64 [E * R * T_max])
+    meaning row r is pool[row_map[r]]; values as for ``dispatch``.
+    Returns (out [R, T, H] in the payload type's storage, flag_words int64 [R, E]).
     """
+    code, es, npdt = DTYPES[dtype]
     idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
     w = np.ascontiguousarray(topk_w, dtype=np.float32)
     R, T, K = idx.shape
     assert w.shape == (R, T, K)
     T_max = T if num_max_tokens is None else num_max_tokens
-    nrows = num_experts * R * T_max
-    if isinstance(y_rows, tuple):
-        pool, row_map = y_rows
-        pool = np.ascontiguousarray(pool, dtype=np.uint16)
-        row_map = np.ascontiguousarray(row_map, dtype=np.int64)
-        assert pool.shape[1] == hidden and row_map.shape == (nrows,)
-        ptrs = (pool.ctypes.data + row_map * (2 * hidden)).astype(np.uint64)
-        keep = pool
-    else:
-        dense = np.ascontiguousarray(y_rows, dtype=np.uint16)
-        assert dense.shape == (nrows, hidden)
-        ptrs = (dense.ctypes.data + np.arange(nrows, dtype=np.uint64) * np.uint64(2 * hidden)).astype(np.uint64)
-        keep = dense
-    out = np.empty((R, T, hidden), dtype=np.uint16)
+    ptrs, keep = _row_pointers(y_rows, hidden, num_experts * R * T_max, dtype)
+    out = np.empty((R, T, hidden), dtype=npdt)
     flag_words = np.empty((R, num_experts), dtype=np.int64)
-    rc = lib().oracle_combine(R, T_max, T, hidden, num_experts, K, _ptr(ptrs), _ptr(idx), _ptr(w),
+    rc = lib().oracle_combine(R, T_max, T, hidden, num_experts, K, code, _ptr(ptrs), _ptr(idx), _ptr(w),
                               _ptr(out), _ptr(flag_words))
     del keep
     if rc != OK:
@@ -238,36 +254,38 @@ def combine(y_rows, topk_idx: np.ndarray, topk_w: np.ndarray, hidden: int, num_e
     return out, flag_words
 
 
-def _row_pointers(y_rows, hidden: int, nrows: int):
+def _row_pointers(y_rows, hidden: int, nrows: int, dtype: str = "bf16"):
+    _, es, npdt = DTYPES[dtype]
     if isinstance(y_rows, tuple):
         pool, row_map = y_rows
-        pool = np.ascontiguousarray(pool, dtype=np.uint16)
+        pool = np.ascontiguousarray(pool, dtype=npdt)
         row_map = np.ascontiguousarray(row_map, dtype=np.int64)
         assert pool.shape[1] == hidden and row_map.shape == (nrows,)
-        return (pool.ctypes.data + row_map * (2 * hidden)).astype(np.uint64), pool
-    dense = np.ascontiguousarray(y_rows, dtype=np.uint16)
+        return (pool.ctypes.data + row_map * (es * hidden)).astype(np.uint64), pool
+    dense = np.ascontiguousarray(y_rows, dtype=npdt)
     assert dense.shape == (nrows, hidden)
-    return (dense.ctypes.data + np.arange(nrows, dtype=np.uint64) * np.uint64(2 * hidden)).astype(np.uint64), dense
+    return (dense.ctypes.data + np.arange(nrows, dtype=np.uint64) * np.uint64(es * hidden)).astype(np.uint64), dense
 
 
 def combine_staged(y_rows, topk_idx: np.ndarray, topk_w: np.ndarray, hidden: int, num_experts: int,
-                   num_max_tokens: int | None = None):
+                   num_max_tokens: int | None = None, dtype: str = "bf16"):
     """Expected staged combine: dict with msg_rank [n], msg_row [n] (row of
-    the source rank's combine receive region), msgs uint8 [n, 4 + 2H],
-    out uint16 [R, T, H], flag_words int64 [R, E]."""
+    the source rank's combine receive region), msgs uint8 [n, 4 + H*size],
+    out [R, T, H], flag_words int64 [R, E]."""
+    code, es, npdt = DTYPES[dtype]
     idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
     w = np.ascontiguousarray(topk_w, dtype=np.float32)
     R, T, K = idx.shape
     T_max = T if num_max_tokens is None else num_max_tokens
-    ptrs, keep = _row_pointers(y_rows, hidden, num_experts * R * T_max)
+    ptrs, keep = _row_pointers(y_rows, hidden, num_experts * R * T_max, dtype)
     cap = max(R * T * K, 1)
     msg_rank = np.empty(cap, dtype=np.int64)
     msg_row = np.empty(cap, dtype=np.int64)
-    msgs = np.empty((cap, 4 + 2 * hidden), dtype=np.uint8)
-    out = np.empty((R, T, hidden), dtype=np.uint16)
+    msgs = np.empty((cap, 4 + es * hidden), dtype=np.uint8)
+    out = np.empty((R, T, hidden), dtype=npdt)
     flag_words = np.empty((R, num_experts), dtype=np.int64)
     n = ctypes.c_int64(0)
-    rc = lib().oracle_combine_staged(R, T_max, T, hidden, num_experts, K, _ptr(ptrs), _ptr(idx), _ptr(w),
+    rc = lib().oracle_combine_staged(R, T_max, T, hidden, num_experts, K, code, _ptr(ptrs), _ptr(idx), _ptr(w),
                                      _ptr(msg_rank), _ptr(msg_row), _ptr(msgs), _ptr(out), _ptr(flag_words),
                                      ctypes.addressof(n))
     del keep

@@ -34,6 +34,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 
 #define ORACLE_OK 0
 #define ORACLE_BAD_EXPERT 1   /* an id outside [-1, num_experts) */
@@ -69,6 +70,94 @@ uint16_t oracle_f32_to_bf16(float f) {
 
 void oracle_f32_to_bf16_array(const float* f, uint16_t* b, int64_t n) {
   for (int64_t i = 0; i < n; ++i) b[i] = oracle_f32_to_bf16(f[i]);
+}
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits.  Widening to binary32 is exact. */
+float oracle_f16_to_f32(uint16_t h) {
+  uint32_t sign = (uint32_t)(h >> 15) << 31;
+  uint32_t exp = (h >> 10) & 0x1fu, frac = h & 0x3ffu, u;
+  if (exp == 0) {
+    /* zero or subnormal: frac * 2^-24, exact in binary32 */
+    float mag = (float)frac * 5.9604644775390625e-08f;
+    float f = sign ? -mag : mag;
+    return f;
+  }
+  if (exp == 31) {
+    u = sign | 0x7f800000u | (frac << 13); /* inf or NaN */
+  } else {
+    u = sign | ((exp - 15 + 127) << 23) | (frac << 13);
+  }
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Round half to even of a non-negative value below 2^24 that is an integer
+ * plus a fraction representable in binary32 (as every value scaled here is). */
+static uint32_t round_half_even_u(float q) {
+  float fl = (float)(uint32_t)q; /* truncation = floor for q >= 0 */
+  float r = q - fl;              /* exact */
+  uint32_t n = (uint32_t)fl;
+  if (r > 0.5f || (r == 0.5f && (n & 1u))) n += 1u;
+  return n;
+}
+
+/* binary32 -> binary16, round to nearest, ties to even; overflow to
+ * infinity; NaN stays NaN. */
+uint16_t oracle_f32_to_f16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)(sign | 0x7e00u);
+  float a = fabsf(f);
+  if (a >= 65520.0f) return (uint16_t)(sign | 0x7c00u); /* at or past the midpoint above 65504 */
+  if (a < 6.103515625e-05f) {                           /* below 2^-14: subnormal step 2^-24 */
+    uint32_t n = round_half_even_u(a * 16777216.0f);    /* a / 2^-24, exact scaling */
+    return (uint16_t)(sign | n);                        /* n == 1024 is the smallest normal */
+  }
+  int e;
+  float m = frexpf(a, &e);               /* a = m * 2^e, m in [0.5, 1) */
+  int exp = e - 1;                       /* a = (2m) * 2^exp, 2m in [1, 2) */
+  float q = (2.0f * m - 1.0f) * 1024.0f; /* fraction scaled to 10 bits, exact */
+  uint32_t n = round_half_even_u(q);
+  if (n == 1024u) {
+    n = 0;
+    exp += 1;
+  }
+  if (exp + 15 >= 31) return (uint16_t)(sign | 0x7c00u);
+  return (uint16_t)(sign | ((uint32_t)(exp + 15) << 10) | n);
+}
+
+void oracle_f32_to_f16_array(const float* f, uint16_t* h, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) h[i] = oracle_f32_to_f16(f[i]);
+}
+
+/* Payload element types: LLMoEBufferLayout<T> with T = bf16, fp16 or fp32. */
+#define ORACLE_DT_BF16 0
+#define ORACLE_DT_FP16 1
+#define ORACLE_DT_FP32 2
+
+static int elem_size(int dt) { return dt == ORACLE_DT_FP32 ? 4 : 2; }
+
+static float load_elem(const uint8_t* p, int dt) {
+  if (dt == ORACLE_DT_FP32) {
+    float f;
+    memcpy(&f, p, 4);
+    return f;
+  }
+  uint16_t b;
+  memcpy(&b, p, 2);
+  return dt == ORACLE_DT_FP16 ? oracle_f16_to_f32(b) : oracle_bf16_to_f32(b);
+}
+
+static void store_elem(uint8_t* p, float v, int dt) {
+  if (dt == ORACLE_DT_FP32) {
+    memcpy(p, &v, 4);
+    return;
+  }
+  uint16_t b = dt == ORACLE_DT_FP16 ? oracle_f32_to_f16(v) : oracle_f32_to_bf16(v);
+  memcpy(p, &b, 2);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -227,8 +316,8 @@ int oracle_route(int R, int T, int K, int E, const int64_t* idx, int32_t* slot, 
  * the rows that are written).  Experts are owned in contiguous blocks: with
  * L = E / R local experts per rank, expert e lives on rank dst = e / L as
  * local expert le = e % L.  The unmasked entry (src, t, k) becomes one
- * message [int32 t][x[src][t][0..H) as bf16] (the int header is read as the
- * source token index) at row (le * R + src) * T_max + slot of rank dst's
+ * message [int32 t][x[src][t][0..H) as T] (the int header is read as the
+ * source token index; T is bf16, fp16 or fp32, so 4 + H * sizeof(T) bytes) at row (le * R + src) * T_max + slot of rank dst's
  * dispatch receive region, i.e. recv[le][src][slot] with T_max rows per
  * (le, src) pair: the num_experts * num_tokens rows of the header's recv
  * buffer.  Word le * R + src of rank dst's recv-count words receives the
@@ -239,7 +328,7 @@ int oracle_route(int R, int T, int K, int E, const int64_t* idx, int32_t* slot, 
  *   msgs[n][4 + 2H]                     its bytes,
  *   count_words[R][E]                   rank r's E count words.
  * Returns ORACLE_OK or an input error; *n_out receives n. */
-int oracle_dispatch(int R, int T_max, int T, int H, int E, int K, const uint16_t* x, const int64_t* idx,
+int oracle_dispatch(int R, int T_max, int T, int H, int E, int K, int dtype, const uint8_t* x, const int64_t* idx,
                     int64_t* row_rank, int64_t* row_index, uint8_t* msgs, int64_t* count_words,
                     int64_t* n_out) {
   *n_out = 0;
@@ -259,7 +348,8 @@ int oracle_dispatch(int R, int T_max, int T, int H, int E, int K, const uint16_t
     return rc;
   }
   const int L = E / R;
-  const size_t msg = 4 + 2 * (size_t)H;
+  const size_t row_bytes = (size_t)H * elem_size(dtype);
+  const size_t msg = 4 + row_bytes;
   int64_t n = 0;
   for (int src = 0; src < R; ++src) {
     for (int t = 0; t < T; ++t) {
@@ -273,7 +363,7 @@ int oracle_dispatch(int R, int T_max, int T, int H, int E, int K, const uint16_t
         uint8_t* out = msgs + (size_t)n * msg;
         int32_t header = t;
         memcpy(out, &header, 4);
-        memcpy(out + 4, x + ((size_t)src * T + t) * H, 2 * (size_t)H);
+        memcpy(out + 4, x + ((size_t)src * T + t) * row_bytes, row_bytes);
         n += 1;
       }
     }
@@ -294,8 +384,9 @@ int oracle_dispatch(int R, int T_max, int T, int H, int E, int K, const uint16_t
 /* Combine                                                                   */
 /* ------------------------------------------------------------------------ */
 
-/* out[src][t][h] = bf16_rne( sum over k = 0..K-1 ascending, idx != -1, of
- *                            fl32( w[src][t][k] * f32(y_row[h]) ) )
+/* out[src][t][h] = T_rne( sum over k = 0..K-1 ascending, idx != -1, of
+ *                         fl32( w[src][t][k] * f32(y_row[h]) ) )
+ * with T the payload type (bf16 or fp16 rounded to nearest even; fp32 kept)
  * where y_row is the expert output for the row that token's entry occupied
  * in the dispatch: the expert outputs are indexed like the receive rows of all
  * ranks laid end to end, row e * R * T_max + src * T_max + slot.  The
@@ -307,8 +398,8 @@ int oracle_dispatch(int R, int T_max, int T, int H, int E, int K, const uint16_t
  * y_rows[E * R * T_max] holds one pointer per expert-output row (H bf16
  * values); rows that no entry uses are never read and may be NULL.
  * Returns ORACLE_OK or an input error. */
-int oracle_combine(int R, int T_max, int T, int H, int E, int K, const uint16_t* const* y_rows,
-                   const int64_t* idx, const float* w, uint16_t* out, int64_t* flag_words) {
+int oracle_combine(int R, int T_max, int T, int H, int E, int K, int dtype, const uint8_t* const* y_rows,
+                   const int64_t* idx, const float* w, uint8_t* out, int64_t* flag_words) {
   if (R < 1 || T_max < 1 || T < 0 || T > T_max || H < 1 || E < 1 || K < 1 || E % R != 0) return ORACLE_BAD_ARG;
   int64_t ntk = (int64_t)R * T * K;
   int32_t* slot = (int32_t*)malloc((size_t)(ntk > 0 ? ntk : 1) * sizeof(int32_t));
@@ -327,6 +418,7 @@ int oracle_combine(int R, int T_max, int T, int H, int E, int K, const uint16_t*
     free(acc);
     return rc;
   }
+  const size_t es = (size_t)elem_size(dtype);
   for (int src = 0; src < R; ++src) {
     for (int t = 0; t < T; ++t) {
       for (int h = 0; h < H; ++h) acc[h] = 0.0f;
@@ -335,15 +427,15 @@ int oracle_combine(int R, int T_max, int T, int H, int E, int K, const uint16_t*
         int64_t e = idx[pos];
         if (e < 0) continue;
         int64_t row = e * R * T_max + (int64_t)src * T_max + slot[pos];
-        const uint16_t* y = y_rows[row];
+        const uint8_t* y = y_rows[row];
         float wk = w[pos];
         for (int h = 0; h < H; ++h) {
-          float p = wk * oracle_bf16_to_f32(y[h]);
+          float p = wk * load_elem(y + (size_t)h * es, dtype);
           acc[h] = acc[h] + p;
         }
       }
-      uint16_t* o = out + ((size_t)src * T + t) * H;
-      for (int h = 0; h < H; ++h) o[h] = oracle_f32_to_bf16(acc[h]);
+      uint8_t* o = out + ((size_t)src * T + t) * H * es;
+      for (int h = 0; h < H; ++h) store_elem(o + (size_t)h * es, acc[h], dtype);
     }
   }
   for (int src = 0; src < R; ++src)
@@ -371,7 +463,7 @@ void oracle_clean(int R, int E, int64_t* sig_words) {
 
 /* The combine routed through the combine receive buffers.  Step one: every
  * unmasked entry (src, t, k) choosing expert e has its expert output row
- * returned to rank src as one message [int32 t][y_row as bf16] at row
+ * returned to rank src as one message [int32 t][y_row as T] at row
  * e * T_max + t of rank src's combine receive region (combine_recv[e][t]: the
  * num_experts * num_tokens messages the layout sizes that buffer for).
  * Step two: rank src reduces out[src][t] from the payloads of its messages
@@ -380,9 +472,9 @@ void oracle_clean(int R, int E, int64_t* sig_words) {
  *
  * Outputs: msg_rank[n], msg_row[n], msgs[n][4 + 2H] in (src, t, k) order of
  * the unmasked entries, out[R][T][H], flag_words[R][E].  *n_out = n. */
-int oracle_combine_staged(int R, int T_max, int T, int H, int E, int K, const uint16_t* const* y_rows,
+int oracle_combine_staged(int R, int T_max, int T, int H, int E, int K, int dtype, const uint8_t* const* y_rows,
                           const int64_t* idx, const float* w, int64_t* msg_rank, int64_t* msg_row, uint8_t* msgs,
-                          uint16_t* out, int64_t* flag_words, int64_t* n_out) {
+                          uint8_t* out, int64_t* flag_words, int64_t* n_out) {
   *n_out = 0;
   if (R < 1 || T_max < 1 || T < 0 || T > T_max || H < 1 || E < 1 || K < 1 || E % R != 0) return ORACLE_BAD_ARG;
   int64_t ntk = (int64_t)R * T * K;
@@ -399,7 +491,8 @@ int oracle_combine_staged(int R, int T_max, int T, int H, int E, int K, const ui
     free(slot); free(cnt); free(where); free(acc);
     return rc;
   }
-  const size_t msg = 4 + 2 * (size_t)H;
+  const size_t es = (size_t)elem_size(dtype);
+  const size_t msg = 4 + (size_t)H * es;
   /* step one: the returned messages */
   int64_t n = 0;
   for (int src = 0; src < R; ++src) {
@@ -415,7 +508,7 @@ int oracle_combine_staged(int R, int T_max, int T, int H, int E, int K, const ui
         uint8_t* m = msgs + (size_t)n * msg;
         int32_t header = t;
         memcpy(m, &header, 4);
-        memcpy(m + 4, y_rows[yrow], 2 * (size_t)H);
+        memcpy(m + 4, y_rows[yrow], (size_t)H * es);
         where[pos] = n;
         n += 1;
       }
@@ -431,14 +524,12 @@ int oracle_combine_staged(int R, int T_max, int T, int H, int E, int K, const ui
         const uint8_t* payload = msgs + (size_t)where[pos] * msg + 4;
         float wk = w[pos];
         for (int h = 0; h < H; ++h) {
-          uint16_t b;
-          memcpy(&b, payload + 2 * (size_t)h, 2);
-          float p = wk * oracle_bf16_to_f32(b);
+          float p = wk * load_elem(payload + (size_t)h * es, dtype);
           acc[h] = acc[h] + p;
         }
       }
-      uint16_t* o = out + ((size_t)src * T + t) * H;
-      for (int h = 0; h < H; ++h) o[h] = oracle_f32_to_bf16(acc[h]);
+      uint8_t* o = out + ((size_t)src * T + t) * H * es;
+      for (int h = 0; h < H; ++h) store_elem(o + (size_t)h * es, acc[h], dtype);
     }
   }
   for (int src = 0; src < R; ++src)
