@@ -59,6 +59,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="dsv3")
     p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default="bf16", help="payload type T")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -70,7 +71,7 @@ def parse_args(argv=None):
 # algorithmic bytes (per launch / per round)
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(w, n_valid: int, tokens: int) -> dict:
+def algorithmic_bytes(w, n_valid: int, tokens: int, es: int = 2) -> dict:
     """Bytes the path must move, no re-reads or staging counted.
 
     dispatch = x read + top-k ids read + N messages written + R*E count words
@@ -78,8 +79,9 @@ def algorithmic_bytes(w, n_valid: int, tokens: int) -> dict:
     clean    = R*E signal words per set
     """
     R, H, E, K = w.R, w.H, w.E, w.K
-    disp = R * tokens * 2 * H + R * tokens * K * 8 + n_valid * (4 + 2 * H) + R * E * 8
-    comb = R * tokens * K * 12 + n_valid * 2 * H + R * tokens * 2 * H + R * E * 8
+    row = es * H
+    disp = R * tokens * row + R * tokens * K * 8 + n_valid * (4 + row) + R * E * 8
+    comb = R * tokens * K * 12 + n_valid * row + R * tokens * row + R * E * 8
     clean = R * E * 8
     return {"dispatch": disp, "combine": comb, "clean": clean, "round": disp + comb + 2 * clean}
 
@@ -300,16 +302,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     w = WORKLOADS[args.workload]
-    inp = make_inputs(w, seed=args.seed)
+    inp = make_inputs(w, seed=args.seed, dtype=args.dtype)
     tokens = w.T
     n_valid = int((inp["topk_idx"] >= 0).sum())
-    algo = algorithmic_bytes(w, n_valid, tokens)
+    es = 4 if args.dtype == "fp32" else 2
+    algo = algorithmic_bytes(w, n_valid, tokens, es)
 
     dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
     x, idx, wt = dev(inp["x"]), dev(inp["topk_idx"]), dev(inp["topk_w"])
     y = dev(inp["y_pool"]).index_select(0, dev(inp["y_row_map"])).contiguous()
-    out = torch.empty((w.R, tokens, w.H), dtype=torch.int16, device="cuda")
-    rb = llmoe.RankBuffers(w.T, w.H, w.R, w.E, fill=0)
+    out = torch.empty((w.R, tokens, w.H), dtype=torch.float32 if es == 4 else torch.int16, device="cuda")
+    rb = llmoe.RankBuffers(w.T, w.H, w.R, w.E, fill=0, dtype=args.dtype)
     # a round is dispatch(set 0) + combine(set 1) with each kernel also
     # zeroing the other set's signal words (the cleans the next calls need,
     # fused: LLMOE_FLAG_CLEAN_OTHER_SET); the combine's routing is ready long
@@ -430,7 +433,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line = {
             "metric": METRIC, "value": round(round_us, 3), "unit": "us/round", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(round_us / 1e3, 6),
-            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": args.dtype,
             "data": "synthetic",
             "config": {"workload": w.name, "shape": w.describe(), "seed": args.seed, "tokens_per_rank": tokens,
                        "unmasked_entries": n_valid, "parallelism": f"replicas{world}",
@@ -448,7 +451,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "dispatch_us": round(d_us, 3), "combine_us": round(c_us, 3),
             "round_us_four_calls": round(statistics.mean(four_ms) * 1e3, 3),
             "staged_combine_us": round(statistics.mean(staged_ms) * 1e3, 3),
-            "staged_combine_gbs": round((algo["combine"] + 2 * n_valid * (4 + 2 * w.H)) /
+            "staged_combine_gbs": round((algo["combine"] + 2 * n_valid * (4 + es * w.H)) /
                                         (statistics.mean(staged_ms) * 1e3) / 1e3, 1),
             "step_us_median": round(statistics.median(step_ms) * 1e3, 3),
             "wall_s": round(timed[1], 3),
@@ -476,7 +479,8 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
     pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
     hx, hidx, hw = pin(inp["x"]), pin(inp["topk_idx"]), pin(inp["topk_w"])
     hy = pin(dense_y(inp))
-    hout = torch.empty((w.R, tokens, w.H), dtype=torch.int16).pin_memory()
+    hout = torch.empty((w.R, tokens, w.H), dtype=torch.float32 if rb.msg_bytes - 4 == 4 * w.H else torch.int16
+                       ).pin_memory()
     hsig = torch.empty((2, w.R, w.E), dtype=torch.int64).pin_memory()
     dx, didx, dw = torch.empty_like(hx, device="cuda"), torch.empty_like(hidx, device="cuda"), torch.empty_like(
         hw, device="cuda")

@@ -26,6 +26,7 @@
 //     round-to-nearest-even store.
 //   clean_kernel: zeroes a set's R * E signal words (LLMoEBuffer::clean_meta).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,7 +50,9 @@ struct Geometry {
   int32_t* err;          // optional error word
   uint32_t flags;        // LLMOE_FLAG_*
   int T_max, T, H, R, E, K, L;
-  int nq;       // 16-byte quads per row, H / 8
+  int dtype;      // LLMOE_DTYPE_*
+  int row_bytes;  // H * element size
+  int nq;       // 16-byte quads per row
   int nchunks;  // warp units per row, ceil(nq / 32)
   int TB;       // tokens per CTA
   int nblk;     // token blocks per source rank
@@ -322,7 +325,7 @@ constexpr int kDspThreads = 32 * (1 + kDspConsumers);
 #endif
 constexpr int kDestRegs = LLMOE_DSP_DEST_REGS > 0 ? LLMOE_DSP_DEST_REGS : 1;  // destinations a dispatch thread keeps in registers
 
-__global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const uint16_t* __restrict__ x,
+__global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const void* __restrict__ x,
                                                                const int64_t* __restrict__ idx) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ring<kDspStages> ring;
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
   const bool last = (b == g.nblk - 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row_bytes = 2 * g.H;
+  const int row_bytes = g.row_bytes;
   const int nch = (row_bytes + kDspChunk - 1) / kDspChunk;
   const int n_iters = (t1 - t0) * nch;
 
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const
   if (!early) wait_prior_grid();
 
   // x does not depend on the routing: start streaming it before the scan
-  const uint8_t* xsrc = reinterpret_cast<const uint8_t*>(x + ((int64_t)src * g.T + t0) * g.H);
+  const uint8_t* xsrc = reinterpret_cast<const uint8_t*>(x) + ((int64_t)src * g.T + t0) * g.row_bytes;
   auto issue = [&](int it) {
     const int tl = it / nch, c = it % nch;
     const int len = min(kDspChunk, row_bytes - c * kDspChunk);
@@ -478,14 +481,62 @@ __device__ __forceinline__ void axpy_quad(float (&acc)[8], float w, const uint4&
 // One warp reduces 32 quads (512 B) of one output row per unit: up to
 // kKBatch expert rows are loaded (16 B per lane each) before they are
 // accumulated, in ascending k.
+// One 16-byte quad of payload values, by payload type: accumulate w * value
+// into acc in fp32 (product rounded, then sum rounded: never fused), and pack
+// the accumulators back (bf16 / fp16 round to nearest even; fp32 kept).
+template <int DT>
+__device__ __forceinline__ void axpy_q(float (&acc)[8], float w, const uint4& v);
+template <>
+__device__ __forceinline__ void axpy_q<LLMOE_DTYPE_BF16>(float (&acc)[8], float w, const uint4& v) {
+  axpy_quad(acc, w, v);
+}
+template <>
+__device__ __forceinline__ void axpy_q<LLMOE_DTYPE_FP16>(float (&acc)[8], float w, const uint4& v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));  // exact
+    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, f.x));
+    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, f.y));
+  }
+}
+template <>
+__device__ __forceinline__ void axpy_q<LLMOE_DTYPE_FP32>(float (&acc)[8], float w, const uint4& v) {
+  acc[0] = __fadd_rn(acc[0], __fmul_rn(w, __uint_as_float(v.x)));
+  acc[1] = __fadd_rn(acc[1], __fmul_rn(w, __uint_as_float(v.y)));
+  acc[2] = __fadd_rn(acc[2], __fmul_rn(w, __uint_as_float(v.z)));
+  acc[3] = __fadd_rn(acc[3], __fmul_rn(w, __uint_as_float(v.w)));
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack_q(const float (&acc)[8]) {
+  if constexpr (DT == LLMOE_DTYPE_FP32) {
+    return make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                      __float_as_uint(acc[3]));
+  } else {
+    uint32_t u[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (DT == LLMOE_DTYPE_FP16) {
+        const __half2 h = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+        u[i] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        u[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+      }
+    }
+    return make_uint4(u[0], u[1], u[2], u[3]);
+  }
+}
+
 constexpr int kCmbThreads = LLMOE_CMB_THREADS;
 constexpr int kCmbWarps = kCmbThreads / 32;
 constexpr int kKBatch = 8;
 
-__global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const uint16_t* __restrict__ y,
+template <int DT>
+__global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const void* __restrict__ y,
                                                               const int64_t* __restrict__ idx,
                                                               const float* __restrict__ topk_w,
-                                                              uint16_t* __restrict__ out) {
+                                                              void* __restrict__ out) {
   extern __shared__ __align__(128) unsigned char smem[];
   const RouteSmem s = carve_route(smem, g);
   const int TBK = g.TB * g.K;
@@ -508,7 +559,7 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
     const uint4* r = nullptr;
     if (sl >= 0) {
       const uint64_t row = (uint64_t)e * g.R * g.T_max + (uint64_t)src * g.T_max + sl;
-      r = reinterpret_cast<const uint4*>(y + row * g.H);
+      r = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(y) + row * g.row_bytes);
     }
     s_row[q] = r;
     s_w[q] = q == threadIdx.x ? w0 : wblk[q];
@@ -541,15 +592,11 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
 #pragma unroll
       for (int i = 0; i < kKBatch; ++i) {
         const int k = k0 + i;
-        if (k < g.K && rows[k] != nullptr) axpy_quad(acc, ws[k], v[i]);
+        if (k < g.K && rows[k] != nullptr) axpy_q<DT>(acc, ws[k], v[i]);
       }
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    reinterpret_cast<uint4*>(out + ((int64_t)src * g.T + t) * g.H)[j] = o;
+    reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + ((int64_t)src * g.T + t) * g.row_bytes)[j] =
+        pack_q<DT>(acc);
   }
 
   if (last) {
@@ -588,7 +635,7 @@ __device__ __forceinline__ uint4 unshift_words(const uint4& a, const uint4& b, i
 // combine_recv[e][t] (row e * T_max + t of its receive region).  One warp
 // moves 32 quads of one entry's row per unit; rank src's flag words are
 // written by the CTA of its last token block.
-__global__ void __launch_bounds__(kThreads) combine_put_kernel(Geometry g, const uint16_t* __restrict__ y,
+__global__ void __launch_bounds__(kThreads) combine_put_kernel(Geometry g, const void* __restrict__ y,
                                                                const int64_t* __restrict__ idx) {
   extern __shared__ __align__(128) unsigned char smem[];
   const RouteSmem s = carve_route(smem, g);
@@ -611,7 +658,8 @@ __global__ void __launch_bounds__(kThreads) combine_put_kernel(Geometry g, const
     const uint4* row = nullptr;
     uintptr_t d = 0;
     if (sl >= 0) {
-      row = reinterpret_cast<const uint4*>(y + ((uint64_t)e * g.R * g.T_max + (uint64_t)src * g.T_max + sl) * g.H);
+      row = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(y) +
+                                           ((uint64_t)e * g.R * g.T_max + (uint64_t)src * g.T_max + sl) * g.row_bytes);
       d = pack_dest(rbase + ((uint64_t)e * g.T_max + (t0 + q / g.K)) * g.msg);
     }
     s_src[q] = row;
@@ -647,9 +695,10 @@ __global__ void __launch_bounds__(kThreads) combine_put_kernel(Geometry g, const
 // One warp per (token, 32-quad chunk); the messages sit at 4-byte phases, so
 // each lane loads its aligned quad, takes the next one from its neighbour and
 // shifts the payload words into place.
+template <int DT>
 __global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, const int64_t* __restrict__ idx,
                                                                   const float* __restrict__ topk_w,
-                                                                  uint16_t* __restrict__ out) {
+                                                                  void* __restrict__ out) {
   release_next_grid();
   wait_prior_grid();
   const int lane = threadIdx.x & 31;
@@ -686,16 +735,11 @@ __global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, co
       if (lane == 31 && phase != 0 && j < g.nq) b = __ldg(qb + j + 1);
       if (g.err != nullptr && j == 0 && *reinterpret_cast<const int32_t*>(msg) != t)
         report(g.err, LLMOE_DEV_BAD_MESSAGE);
-      if (j < g.nq) axpy_quad(acc, wk, unshift_words(a, b, phase));
+      if (j < g.nq) axpy_q<DT>(acc, wk, unshift_words(a, b, phase));
     }
-    if (j < g.nq) {
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      reinterpret_cast<uint4*>(out + ((int64_t)src * g.T + t) * g.H)[j] = o;
-    }
+    if (j < g.nq)
+      reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + ((int64_t)src * g.T + t) * g.row_bytes)[j] =
+          pack_q<DT>(acc);
   }
 }
 
@@ -743,12 +787,12 @@ struct LayoutInfo {
   uint64_t total, msg, send, recv, sig;
 };
 
-// LLMoEBufferLayout<bf16>: send = max(T*msg, E*T*msg), recv = E*T*msg (both
-// roles), sig = 8*E; each region twice; msg = sizeof(int) + 2*hidden.
-bool layout_info(int T, int H, int R, int E, LayoutInfo* out) {
-  if (T < 1 || H < 1 || R < 1 || E < 1) return false;
+// LLMoEBufferLayout<T>: send = max(T*msg, E*T*msg), recv = E*T*msg (both
+// roles), sig = 8*E; each region twice; msg = sizeof(int) + hidden*sizeof(T).
+bool layout_info(int T, int H, int R, int E, int es, LayoutInfo* out) {
+  if (T < 1 || H < 1 || R < 1 || E < 1 || es < 1) return false;
   uint64_t msg, et, dsend, csend, recv, total = 0, two;
-  if (!mul_u64((uint64_t)H, 2, &msg) || !add_u64(msg, 4, &msg)) return false;
+  if (!mul_u64((uint64_t)H, (uint64_t)es, &msg) || !add_u64(msg, 4, &msg)) return false;
   if (!mul_u64((uint64_t)T, msg, &dsend)) return false;
   if (!mul_u64((uint64_t)E, (uint64_t)T, &et) || !mul_u64(et, msg, &csend)) return false;
   const uint64_t send = dsend > csend ? dsend : csend;
@@ -760,6 +804,15 @@ bool layout_info(int T, int H, int R, int E, LayoutInfo* out) {
   if (!add_u64(total, 2 * sig, &total)) return false;
   *out = LayoutInfo{total, msg, send, recv, sig};
   return true;
+}
+
+int dtype_size(int dtype) {
+  switch (dtype) {
+    case LLMOE_DTYPE_BF16: return 2;
+    case LLMOE_DTYPE_FP16: return 2;
+    case LLMOE_DTYPE_FP32: return 4;
+    default: return 0;
+  }
 }
 
 int g_num_sms[64] = {0};
@@ -782,18 +835,19 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   if (bs == nullptr) return LLMOE_ERR_INVALID_ARGUMENT;
   const int T_max = bs->num_max_tokens, T = bs->num_tokens, H = bs->hidden, R = bs->num_ranks,
             E = bs->num_experts, K = bs->num_topk;
-  if (T_max < 1 || T < 0 || T > T_max || H < 8 || H % 8 != 0 || R < 1 || E < R || E % R != 0 ||
-      E > LLMOE_MAX_EXPERTS || K < 1 || K > LLMOE_MAX_TOPK || K > E)
+  const int es = dtype_size(bs->dtype);
+  if (es == 0 || T_max < 1 || T < 0 || T > T_max || H < 1 || ((int64_t)H * es) % 16 != 0 || R < 1 || E < R ||
+      E % R != 0 || E > LLMOE_MAX_EXPERTS || K < 1 || K > LLMOE_MAX_TOPK || K > E)
     return LLMOE_ERR_INVALID_ARGUMENT;
   const int set = need_buffers ? bs->set : 0;
   if (set != 0 && set != 1) return LLMOE_ERR_INVALID_ARGUMENT;
   if (bs->err != nullptr && !aligned(bs->err, 4)) return LLMOE_ERR_INVALID_ARGUMENT;
   LayoutInfo li;
-  if (!layout_info(T_max, H, R, E, &li)) return LLMOE_ERR_INVALID_ARGUMENT;
+  if (!layout_info(T_max, H, R, E, es, &li)) return LLMOE_ERR_INVALID_ARGUMENT;
   // every index the kernels form stays below 2^63
-  uint64_t rows, elems;
-  if (!mul_u64((uint64_t)E * (uint64_t)R, (uint64_t)T_max, &rows) || !mul_u64(rows, (uint64_t)H, &elems) ||
-      elems > (uint64_t)INT64_MAX / 2)
+  uint64_t rows, bytes;
+  if (!mul_u64((uint64_t)E * (uint64_t)R, (uint64_t)T_max, &rows) || !mul_u64(rows, (uint64_t)H * es, &bytes) ||
+      bytes > (uint64_t)INT64_MAX / 2)
     return LLMOE_ERR_INVALID_ARGUMENT;
   if (need_buffers) {
     uint64_t span;
@@ -816,7 +870,9 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   g->E = E;
   g->K = K;
   g->L = E / R;
-  g->nq = H / 8;
+  g->dtype = bs->dtype;
+  g->row_bytes = H * es;
+  g->nq = g->row_bytes / 16;
   g->nchunks = (g->nq + 31) / 32;
   g->TB = 1;
   g->nblk = T > 0 ? T : 1;
@@ -835,7 +891,7 @@ void set_blocking(Geometry* g, int blocks_per_sm) {
   g->nblk = g->T > 0 ? (g->T + g->TB - 1) / g->TB : 1;
 }
 
-int g_smem_optin[64][8] = {{0}};
+int g_smem_optin[64][32] = {{0}};
 
 // Opts a kernel in to more than 48 KB of dynamic shared memory (once per
 // device and size).
@@ -860,11 +916,14 @@ enum KernelId {
   kCombineReduceKernel = 4,
   kNumKernels = 5
 };
-int g_occupancy[64][kNumKernels] = {{0}};
+int g_occupancy[64][32] = {{0}};
+
+// Cache slot of a kernel instantiation: kernel id and payload type.
+int kslot(KernelId id, int dtype = 0) { return (int)id * 4 + dtype; }
 
 // Resident CTAs per SM of a kernel at kThreads threads and `smem` bytes,
 // cached per device.
-int blocks_per_sm(KernelId id, const void* fn, int threads, size_t smem) {
+int blocks_per_sm(int id, const void* fn, int threads, size_t smem) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
   if (dev < 64 && g_occupancy[dev][id] > 0) return g_occupancy[dev][id];
@@ -913,19 +972,51 @@ int launch(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
   return LLMOE_SUCCESS;
 }
 
+template <int DT>
+int launch_combine(Geometry& g, const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
+                   llmoe_stream_t stream) {
+  const int id = kslot(kCombineKernel, DT);
+  set_blocking(&g, blocks_per_sm(id, (const void*)combine_kernel<DT>, kCmbThreads, combine_smem_bytes(g)));
+  const size_t smem = combine_smem_bytes(g);
+  const int rc = set_smem(id, (const void*)combine_kernel<DT>, smem);
+  if (rc != LLMOE_SUCCESS) return rc;
+  return launch(combine_kernel<DT>, g.R * g.nblk, kCmbThreads, smem, stream, g, y, topk_idx, topk_w, out);
+}
+
+template <int DT>
+int launch_reduce(const Geometry& g, const int64_t* topk_idx, const float* topk_w, void* out, llmoe_stream_t stream) {
+  const int64_t warps = (int64_t)g.R * g.T * g.nchunks;
+  const int64_t wave = (int64_t)num_sms() * blocks_per_sm(kslot(kCombineReduceKernel, DT),
+                                                          (const void*)combine_reduce_kernel<DT>, kThreads, 0);
+  const int64_t blocks = std::min<int64_t>(wave, (warps + kThreads / 32 - 1) / (kThreads / 32));
+  return launch(combine_reduce_kernel<DT>, (unsigned)blocks, kThreads, 0, stream, g, topk_idx, topk_w, out);
+}
+
 }  // namespace
 
 extern "C" {
 
-size_t llmoe_layout_bytes(int num_max_tokens, int hidden, int num_ranks, int num_experts) {
+size_t llmoe_layout_bytes_dtype(int num_max_tokens, int hidden, int num_ranks, int num_experts, int dtype) {
   LayoutInfo li;
-  return layout_info(num_max_tokens, hidden, num_ranks, num_experts, &li) ? (size_t)li.total : 0;
+  const int es = dtype_size(dtype);
+  return es && layout_info(num_max_tokens, hidden, num_ranks, num_experts, es, &li) ? (size_t)li.total : 0;
+}
+
+size_t llmoe_layout_bytes(int num_max_tokens, int hidden, int num_ranks, int num_experts) {
+  return llmoe_layout_bytes_dtype(num_max_tokens, hidden, num_ranks, num_experts, LLMOE_DTYPE_BF16);
 }
 
 int llmoe_layout_offsets(int num_max_tokens, int hidden, int num_ranks, int num_experts, int set,
                          uint64_t* send_offset, uint64_t* recv_offset, uint64_t* signal_offset) {
+  return llmoe_layout_offsets_dtype(num_max_tokens, hidden, num_ranks, num_experts, LLMOE_DTYPE_BF16, set,
+                                    send_offset, recv_offset, signal_offset);
+}
+
+int llmoe_layout_offsets_dtype(int num_max_tokens, int hidden, int num_ranks, int num_experts, int dtype, int set,
+                               uint64_t* send_offset, uint64_t* recv_offset, uint64_t* signal_offset) {
   LayoutInfo li;
-  if ((set != 0 && set != 1) || !layout_info(num_max_tokens, hidden, num_ranks, num_experts, &li))
+  const int es = dtype_size(dtype);
+  if ((set != 0 && set != 1) || es == 0 || !layout_info(num_max_tokens, hidden, num_ranks, num_experts, es, &li))
     return LLMOE_ERR_INVALID_ARGUMENT;
   if (send_offset) *send_offset = li.send * (uint64_t)set;
   if (recv_offset) *recv_offset = 2 * li.send + li.recv * (uint64_t)set;
@@ -941,25 +1032,25 @@ int llmoe_route(const int64_t* topk_idx, int32_t* slot, int64_t* counts, const l
   if (counts == nullptr || !aligned(counts, 8)) return LLMOE_ERR_INVALID_ARGUMENT;
   if (g.T > 0 && (topk_idx == nullptr || slot == nullptr || !aligned(topk_idx, 8) || !aligned(slot, 4)))
     return LLMOE_ERR_INVALID_ARGUMENT;
-  set_blocking(&g, blocks_per_sm(kRouteKernel, (const void*)route_kernel, kThreads, route_smem_bytes(g)));
+  set_blocking(&g, blocks_per_sm(kslot(kRouteKernel), (const void*)route_kernel, kThreads, route_smem_bytes(g)));
   const size_t smem = route_smem_bytes(g);
-  if ((rc = set_smem(kRouteKernel, (const void*)route_kernel, smem)) != LLMOE_SUCCESS) return rc;
+  if ((rc = set_smem(kslot(kRouteKernel), (const void*)route_kernel, smem)) != LLMOE_SUCCESS) return rc;
   return launch(route_kernel, g.R * g.nblk, kThreads, smem, stream, g, topk_idx, slot, counts);
 }
 
-int llmoe_dispatch(const uint16_t* x, const int64_t* topk_idx, const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
+int llmoe_dispatch(const void* x, const int64_t* topk_idx, const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
   Geometry g;
   int rc = make_geometry(bs, true, &g);
   if (rc != LLMOE_SUCCESS) return rc;
   if (g.T > 0 && (x == nullptr || topk_idx == nullptr || !aligned(x, 16) || !aligned(topk_idx, 8)))
     return LLMOE_ERR_INVALID_ARGUMENT;
-  set_blocking(&g, blocks_per_sm(kDispatchKernel, (const void*)dispatch_kernel, kDspThreads, dispatch_smem_bytes(g)));
+  set_blocking(&g, blocks_per_sm(kslot(kDispatchKernel), (const void*)dispatch_kernel, kDspThreads, dispatch_smem_bytes(g)));
   const size_t smem = dispatch_smem_bytes(g);
-  if ((rc = set_smem(kDispatchKernel, (const void*)dispatch_kernel, smem)) != LLMOE_SUCCESS) return rc;
+  if ((rc = set_smem(kslot(kDispatchKernel), (const void*)dispatch_kernel, smem)) != LLMOE_SUCCESS) return rc;
   return launch(dispatch_kernel, g.R * g.nblk, kDspThreads, smem, stream, g, x, topk_idx);
 }
 
-int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
+int llmoe_combine(const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                   const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
   Geometry g;
   int rc = make_geometry(bs, true, &g);
@@ -970,16 +1061,17 @@ int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const float* topk_
   if (g.T > 0) {
     // out must not overlap y
     const uintptr_t yb = reinterpret_cast<uintptr_t>(y), ob = reinterpret_cast<uintptr_t>(out);
-    const uintptr_t ye = yb + (uintptr_t)g.E * g.R * g.T_max * g.H * 2, oe = ob + (uintptr_t)g.R * g.T * g.H * 2;
+    const uintptr_t ye = yb + (uintptr_t)g.E * g.R * g.T_max * g.row_bytes, oe = ob + (uintptr_t)g.R * g.T * g.row_bytes;
     if (ob < ye && yb < oe) return LLMOE_ERR_INVALID_ARGUMENT;
   }
-  set_blocking(&g, blocks_per_sm(kCombineKernel, (const void*)combine_kernel, kCmbThreads, combine_smem_bytes(g)));
-  const size_t smem = combine_smem_bytes(g);
-  if ((rc = set_smem(kCombineKernel, (const void*)combine_kernel, smem)) != LLMOE_SUCCESS) return rc;
-  return launch(combine_kernel, g.R * g.nblk, kCmbThreads, smem, stream, g, y, topk_idx, topk_w, out);
+  switch (g.dtype) {
+    case LLMOE_DTYPE_FP16: return launch_combine<LLMOE_DTYPE_FP16>(g, y, topk_idx, topk_w, out, stream);
+    case LLMOE_DTYPE_FP32: return launch_combine<LLMOE_DTYPE_FP32>(g, y, topk_idx, topk_w, out, stream);
+    default: return launch_combine<LLMOE_DTYPE_BF16>(g, y, topk_idx, topk_w, out, stream);
+  }
 }
 
-int llmoe_combine_staged(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
+int llmoe_combine_staged(const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                          const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
   Geometry g;
   int rc = make_geometry(bs, true, &g);
@@ -989,24 +1081,24 @@ int llmoe_combine_staged(const uint16_t* y, const int64_t* topk_idx, const float
     return LLMOE_ERR_INVALID_ARGUMENT;
   if (g.T > 0) {
     const uintptr_t yb = reinterpret_cast<uintptr_t>(y), ob = reinterpret_cast<uintptr_t>(out);
-    const uintptr_t ye = yb + (uintptr_t)g.E * g.R * g.T_max * g.H * 2, oe = ob + (uintptr_t)g.R * g.T * g.H * 2;
+    const uintptr_t ye = yb + (uintptr_t)g.E * g.R * g.T_max * g.row_bytes, oe = ob + (uintptr_t)g.R * g.T * g.row_bytes;
     if (ob < ye && yb < oe) return LLMOE_ERR_INVALID_ARGUMENT;
   }
   const size_t put_extra = (sizeof(void*) + sizeof(uintptr_t)) * (size_t)g.K;
-  set_blocking(&g, blocks_per_sm(kCombinePutKernel, (const void*)combine_put_kernel, kThreads,
+  set_blocking(&g, blocks_per_sm(kslot(kCombinePutKernel), (const void*)combine_put_kernel, kThreads,
                                  route_smem_bytes(g) + put_extra));
   const size_t smem = route_smem_bytes(g) + (sizeof(void*) + sizeof(uintptr_t)) * (size_t)g.TB * g.K;
-  if ((rc = set_smem(kCombinePutKernel, (const void*)combine_put_kernel, smem)) != LLMOE_SUCCESS) return rc;
+  if ((rc = set_smem(kslot(kCombinePutKernel), (const void*)combine_put_kernel, smem)) != LLMOE_SUCCESS) return rc;
   if ((rc = launch(combine_put_kernel, g.R * g.nblk, kThreads, smem, stream, g, y, topk_idx)) != LLMOE_SUCCESS)
     return rc;
   if (g.T == 0) return LLMOE_SUCCESS;
-  const int64_t warps = (int64_t)g.R * g.T * g.nchunks;
-  const int64_t wave = (int64_t)num_sms() * blocks_per_sm(kCombineReduceKernel, (const void*)combine_reduce_kernel,
-                                                          kThreads, 0);
-  const int64_t blocks = std::min<int64_t>(wave, (warps + kThreads / 32 - 1) / (kThreads / 32));
   Geometry gr = g;
   gr.flags &= ~LLMOE_FLAG_CLEAN_OTHER_SET;  // the put kernel already cleaned
-  return launch(combine_reduce_kernel, (unsigned)blocks, kThreads, 0, stream, gr, topk_idx, topk_w, out);
+  switch (g.dtype) {
+    case LLMOE_DTYPE_FP16: return launch_reduce<LLMOE_DTYPE_FP16>(gr, topk_idx, topk_w, out, stream);
+    case LLMOE_DTYPE_FP32: return launch_reduce<LLMOE_DTYPE_FP32>(gr, topk_idx, topk_w, out, stream);
+    default: return launch_reduce<LLMOE_DTYPE_BF16>(gr, topk_idx, topk_w, out, stream);
+  }
 }
 
 int llmoe_clean(const llmoe_buf_set_t* bs, llmoe_stream_t stream) {

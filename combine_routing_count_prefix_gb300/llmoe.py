@@ -41,8 +41,13 @@ LLMOE_FLAG_CLEAN_OTHER_SET = 2
 LLMOE_MAX_TOPK = 32
 LLMOE_MAX_EXPERTS = 8192
 
-EXPORTS = ("llmoe_layout_bytes", "llmoe_layout_offsets", "llmoe_route", "llmoe_dispatch", "llmoe_combine",
-           "llmoe_combine_staged", "llmoe_clean", "llmoe_get_error", "llmoe_status_string")
+EXPORTS = ("llmoe_layout_bytes", "llmoe_layout_bytes_dtype", "llmoe_layout_offsets", "llmoe_layout_offsets_dtype",
+           "llmoe_route", "llmoe_dispatch", "llmoe_combine", "llmoe_combine_staged", "llmoe_clean", "llmoe_get_error",
+           "llmoe_status_string")
+
+LLMOE_DTYPE_BF16, LLMOE_DTYPE_FP16, LLMOE_DTYPE_FP32 = 0, 1, 2
+DTYPE_CODES = {"bf16": LLMOE_DTYPE_BF16, "fp16": LLMOE_DTYPE_FP16, "fp32": LLMOE_DTYPE_FP32}
+DTYPE_BYTES = {LLMOE_DTYPE_BF16: 2, LLMOE_DTYPE_FP16: 2, LLMOE_DTYPE_FP32: 4}
 
 
 class llmoe_buf_set_t(ctypes.Structure):
@@ -58,6 +63,7 @@ class llmoe_buf_set_t(ctypes.Structure):
         ("set", ctypes.c_int32),
         ("err", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
+        ("dtype", ctypes.c_int32),
     ]
 
 
@@ -68,6 +74,10 @@ _lib.llmoe_layout_bytes.argtypes = [_I, _I, _I, _I]
 _lib.llmoe_layout_bytes.restype = ctypes.c_size_t
 _lib.llmoe_layout_offsets.argtypes = [_I, _I, _I, _I, _I, _P, _P, _P]
 _lib.llmoe_layout_offsets.restype = _I
+_lib.llmoe_layout_bytes_dtype.argtypes = [_I, _I, _I, _I, _I]
+_lib.llmoe_layout_bytes_dtype.restype = ctypes.c_size_t
+_lib.llmoe_layout_offsets_dtype.argtypes = [_I, _I, _I, _I, _I, _I, _P, _P, _P]
+_lib.llmoe_layout_offsets_dtype.restype = _I
 _lib.llmoe_route.argtypes = [_P, _P, _P, _BS, _P]
 _lib.llmoe_route.restype = _I
 _lib.llmoe_dispatch.argtypes = [_P, _P, _BS, _P]
@@ -96,6 +106,7 @@ def _check(rc: int, call: str) -> None:
 
 
 _DTYPES = {
+    "payload": (torch.bfloat16, torch.float16, torch.int16, torch.uint16, torch.float32),
     "bf16": (torch.bfloat16, torch.int16, torch.uint16),
     "i64": (torch.int64,),
     "i32": (torch.int32,),
@@ -143,24 +154,37 @@ def llmoe_layout_offsets(num_max_tokens: int, hidden: int, num_ranks: int, num_e
     return send.value, recv.value, sig.value
 
 
+def llmoe_layout_bytes_dtype(num_max_tokens: int, hidden: int, num_ranks: int, num_experts: int, dtype: int) -> int:
+    return int(_lib.llmoe_layout_bytes_dtype(num_max_tokens, hidden, num_ranks, num_experts, dtype))
+
+
+def llmoe_layout_offsets_dtype(num_max_tokens: int, hidden: int, num_ranks: int, num_experts: int, dtype: int,
+                               set: int):
+    send, recv, sig = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint64()
+    _check(_lib.llmoe_layout_offsets_dtype(num_max_tokens, hidden, num_ranks, num_experts, dtype, set,
+                                           ctypes.byref(send), ctypes.byref(recv), ctypes.byref(sig)),
+           "llmoe_layout_offsets_dtype")
+    return send.value, recv.value, sig.value
+
+
 def llmoe_route(topk_idx, slot, counts, bs: llmoe_buf_set_t, stream=None) -> None:
     _check(_lib.llmoe_route(_addr(topk_idx, "i64"), _addr(slot, "i32"), _addr(counts, "i64"), ctypes.byref(bs),
                             _stream(stream)), "llmoe_route")
 
 
 def llmoe_dispatch(x, topk_idx, bs: llmoe_buf_set_t, stream=None) -> None:
-    _check(_lib.llmoe_dispatch(_addr(x, "bf16"), _addr(topk_idx, "i64"), ctypes.byref(bs), _stream(stream)),
+    _check(_lib.llmoe_dispatch(_addr(x, "payload"), _addr(topk_idx, "i64"), ctypes.byref(bs), _stream(stream)),
            "llmoe_dispatch")
 
 
 def llmoe_combine(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=None) -> None:
-    _check(_lib.llmoe_combine(_addr(y, "bf16"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"), _addr(out, "bf16"),
+    _check(_lib.llmoe_combine(_addr(y, "payload"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"), _addr(out, "payload"),
                               ctypes.byref(bs), _stream(stream)), "llmoe_combine")
 
 
 def llmoe_combine_staged(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=None) -> None:
-    _check(_lib.llmoe_combine_staged(_addr(y, "bf16"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"),
-                                     _addr(out, "bf16"), ctypes.byref(bs), _stream(stream)), "llmoe_combine_staged")
+    _check(_lib.llmoe_combine_staged(_addr(y, "payload"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"),
+                                     _addr(out, "payload"), ctypes.byref(bs), _stream(stream)), "llmoe_combine_staged")
 
 
 def llmoe_clean(bs: llmoe_buf_set_t, stream=None) -> None:
@@ -193,13 +217,13 @@ class Bound:
 
 
 def bind_dispatch(x, topk_idx, bs: llmoe_buf_set_t, stream=None) -> Bound:
-    return Bound("llmoe_dispatch", (_addr(x, "bf16"), _addr(topk_idx, "i64"), ctypes.byref(bs), _stream(stream)),
+    return Bound("llmoe_dispatch", (_addr(x, "payload"), _addr(topk_idx, "i64"), ctypes.byref(bs), _stream(stream)),
                  (x, topk_idx, bs))
 
 
 def bind_combine(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=None) -> Bound:
-    return Bound("llmoe_combine", (_addr(y, "bf16"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"),
-                                   _addr(out, "bf16"), ctypes.byref(bs), _stream(stream)),
+    return Bound("llmoe_combine", (_addr(y, "payload"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"),
+                                   _addr(out, "payload"), ctypes.byref(bs), _stream(stream)),
                  (y, topk_idx, topk_w, out, bs))
 
 
@@ -219,20 +243,22 @@ class RankBuffers:
     """
 
     def __init__(self, num_max_tokens: int, hidden: int, num_ranks: int, num_experts: int,
-                 device="cuda", guard: int = 0, fill: int | None = None):
+                 device="cuda", guard: int = 0, fill: int | None = None, dtype: str = "bf16"):
         self.T, self.H, self.R, self.E = num_max_tokens, hidden, num_ranks, num_experts
-        self.layout_bytes = llmoe_layout_bytes(num_max_tokens, hidden, num_ranks, num_experts)
+        self.dtype = DTYPE_CODES[dtype]
+        self.layout_bytes = llmoe_layout_bytes_dtype(num_max_tokens, hidden, num_ranks, num_experts, self.dtype)
         if self.layout_bytes == 0:
-            raise LLMoEError(LLMOE_ERR_INVALID_ARGUMENT, "llmoe_layout_bytes")
+            raise LLMoEError(LLMOE_ERR_INVALID_ARGUMENT, "llmoe_layout_bytes_dtype")
         self.rank_stride = round_up(self.layout_bytes + guard, 256)
         self.storage = torch.empty(self.rank_stride * num_ranks, dtype=torch.uint8, device=device)
         if fill is not None:
             self.storage.fill_(fill)
-        self.offsets = [llmoe_layout_offsets(num_max_tokens, hidden, num_ranks, num_experts, s) for s in (0, 1)]
+        self.offsets = [llmoe_layout_offsets_dtype(num_max_tokens, hidden, num_ranks, num_experts, self.dtype, s)
+                        for s in (0, 1)]
 
     @property
     def msg_bytes(self) -> int:
-        return 4 + 2 * self.H
+        return 4 + DTYPE_BYTES[self.dtype] * self.H
 
     def buf_set(self, set: int, num_topk: int, num_tokens: int | None = None, err=None,
                 flags: int = 0) -> llmoe_buf_set_t:
@@ -240,7 +266,7 @@ class RankBuffers:
             base=self.storage.data_ptr(), rank_stride=self.rank_stride, num_max_tokens=self.T,
             num_tokens=self.T if num_tokens is None else num_tokens, hidden=self.H, num_ranks=self.R,
             num_experts=self.E, num_topk=num_topk, set=set, err=None if err is None else _addr(err, "i32"),
-            flags=flags)
+            flags=flags, dtype=self.dtype)
 
     def rank_view(self, r: int) -> torch.Tensor:
         return self.storage[r * self.rank_stride:(r + 1) * self.rank_stride]

@@ -20,7 +20,8 @@
  *     checks are done on the host before any launch: a call that returns
  *     LLMOE_ERR_INVALID_ARGUMENT or LLMOE_ERR_INVALID_USAGE launched nothing.
  *     LLMOE_ERR_CUDA reports a launch error (cudaGetLastError).
- *   - bf16 values travel as their uint16_t bit patterns.
+ *   - Payload values (x, y, out) are of the set's payload type T (bf16 by
+ *     default; fp16 or fp32 through llmoe_buf_set_t.dtype).
  *
  * Sequencing: a set's signal words must be zero before a dispatch or combine
  * writes them (llmoe_clean zeroes them).  A round alternates sets:
@@ -89,6 +90,14 @@ typedef enum {
  * reads the other set's words must do so before this call. */
 #define LLMOE_FLAG_CLEAN_OTHER_SET 2u
 
+/* llmoe_buf_set_t.dtype: the payload type T of LLMoEBufferLayout<T>.  A
+ * message is 4 + hidden * sizeof(T) bytes; hidden * sizeof(T) must be a
+ * multiple of 16.  The combine accumulates in fp32 and stores T (bf16 and
+ * fp16 rounded to nearest even, fp32 as accumulated). */
+#define LLMOE_DTYPE_BF16 0
+#define LLMOE_DTYPE_FP16 1
+#define LLMOE_DTYPE_FP32 2
+
 /* Library limits (checked on the host). */
 #define LLMOE_MAX_TOPK 32
 #define LLMOE_MAX_EXPERTS 8192
@@ -102,7 +111,7 @@ typedef enum {
  *   num_max_tokens T: tokens per rank the layout was sized for (the worst-case
  *                  micro-batch; "num_max_dispatch_tokens_per_rank").
  *   num_tokens     tokens per rank in this call, 0 <= num_tokens <= T.
- *   hidden         H, values per token; a multiple of 8 (16-byte rows).
+ *   hidden         H, values per token; H * sizeof(T) a multiple of 16.
  *   num_ranks      R >= 1.
  *   num_experts    E, a multiple of R, <= LLMOE_MAX_EXPERTS.  Expert e is
  *                  owned by rank e / (E/R) as local expert e % (E/R).
@@ -111,7 +120,8 @@ typedef enum {
  *   err            optional device int32 word; NULL turns validation off.
  *                  With validation off, invalid ids are still skipped and no
  *                  access leaves the buffers, but nothing is reported.
- *   flags          LLMOE_FLAG_* bits; 0 for the plain stream order. */
+ *   flags          LLMOE_FLAG_* bits; 0 for the plain stream order.
+ *   dtype          LLMOE_DTYPE_*: the payload type (0 = bf16). */
 typedef struct {
   void* base;
   uint64_t rank_stride;
@@ -124,6 +134,7 @@ typedef struct {
   int32_t set;
   int32_t* err;
   uint32_t flags;
+  int32_t dtype;
 } llmoe_buf_set_t;
 
 /* Bytes of ONE rank buffer: get_rdma_size_hint<bf16>(num_max_tokens, hidden,
@@ -135,6 +146,9 @@ typedef struct {
  * Host only; touches no device. */
 LLMOE_API size_t llmoe_layout_bytes(int num_max_tokens, int hidden, int num_ranks, int num_experts);
 
+/* The same for payload type `dtype` (LLMOE_DTYPE_*): get_rdma_size_hint<T>. */
+LLMOE_API size_t llmoe_layout_bytes_dtype(int num_max_tokens, int hidden, int num_ranks, int num_experts, int dtype);
+
 /* Byte offsets, from the start of a rank buffer, of buffer set `set`'s send
  * region, receive region and signal words (LLMoEBufferLayout, "Assign
  * pointers"; the combine send / recv / flag of a set are the same addresses
@@ -143,6 +157,11 @@ LLMOE_API size_t llmoe_layout_bytes(int num_max_tokens, int hidden, int num_rank
  * llmoe_layout_bytes would return 0 or set is not 0 or 1. */
 LLMOE_API int llmoe_layout_offsets(int num_max_tokens, int hidden, int num_ranks, int num_experts, int set,
                          uint64_t* send_offset, uint64_t* recv_offset, uint64_t* signal_offset);
+
+/* The same for payload type `dtype` (LLMOE_DTYPE_*). */
+LLMOE_API int llmoe_layout_offsets_dtype(int num_max_tokens, int hidden, int num_ranks, int num_experts, int dtype,
+                                         int set, uint64_t* send_offset, uint64_t* recv_offset,
+                                         uint64_t* signal_offset);
 
 /* Routing count / prefix scan, on its own (dispatch and combine run the same
  * scan inside their kernels and do not need this call).
@@ -158,7 +177,7 @@ LLMOE_API int llmoe_route(const int64_t* topk_idx, int32_t* slot, int64_t* count
                 llmoe_stream_t stream);
 
 /* Dispatch (LLMoEBuffer dispatch receive buffer and recv-count words).
- *   x         device bf16 [R][num_tokens][H], rows 16-byte aligned.
+ *   x         device T [R][num_tokens][H] (T per bs->dtype), 16-byte aligned.
  *   topk_idx  device int64 [R][num_tokens][K], -1 = masked.
  * For every unmasked entry (src, t, k) choosing expert e, owned by rank
  * dst = e / L as local expert le = e % L, writes the message
@@ -167,23 +186,24 @@ LLMOE_API int llmoe_route(const int64_t* topk_idx, int32_t* slot, int64_t* count
  * Then writes rank dst's signal word le * R + src = that bucket's count, for
  * all R * E words.  Nothing else is written: unused receive rows keep their
  * contents. */
-LLMOE_API int llmoe_dispatch(const uint16_t* x, const int64_t* topk_idx, const llmoe_buf_set_t* bs,
+LLMOE_API int llmoe_dispatch(const void* x, const int64_t* topk_idx, const llmoe_buf_set_t* bs,
                    llmoe_stream_t stream);
 
 /* Combine (LLMoEBuffer combine roles; the expert outputs are gathered in
  * place instead of being staged through the combine send / recv regions).
- *   y         device bf16 [E * R * T][H], rows 16-byte aligned: the expert
+ *   y         device T [E * R * T][H], 16-byte aligned: the expert
  *             outputs in receive-row order, row e * R * T + src * T + slot
  *             for the entry that occupied recv[le][src][slot] of rank e / L.
  *   topk_idx  device int64 [R][num_tokens][K], -1 = masked.
  *   topk_w    device fp32 [R][num_tokens][K].
- *   out       device bf16 [R][num_tokens][H] out, rows 16-byte aligned;
+ *   out       device T [R][num_tokens][H] out, 16-byte aligned;
  *             must not overlap y.
- * out[src][t][:] = bf16_rne(sum over ascending k of unmasked entries of
+ * out[src][t][:] = T(sum over ascending k of unmasked entries of
  * fl32(w * fp32(y_row))), starting from +0.0, each product rounded to fp32
- * before it is added (no fused multiply-add).  Then writes rank src's
+ * before it is added (no fused multiply-add); T() rounds to nearest even for
+ * bf16 / fp16.  Then writes rank src's
  * set-`set` signal word e = number of rows expert e returned to src. */
-LLMOE_API int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
+LLMOE_API int llmoe_combine(const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                   const llmoe_buf_set_t* bs, llmoe_stream_t stream);
 
 /* Staged combine (LLMoEBuffer combine receive buffer and recv-flag words): the
@@ -200,7 +220,7 @@ LLMOE_API int llmoe_combine(const uint16_t* y, const int64_t* topk_idx, const fl
  * also checks each message header (LLMOE_DEV_BAD_MESSAGE).  The set's receive
  * region is overwritten at those rows: it aliases the dispatch receive region
  * of the same set. */
-LLMOE_API int llmoe_combine_staged(const uint16_t* y, const int64_t* topk_idx, const float* topk_w, uint16_t* out,
+LLMOE_API int llmoe_combine_staged(const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                                    const llmoe_buf_set_t* bs, llmoe_stream_t stream);
 
 /* Clean (LLMoEBuffer::clean_meta): zero the num_experts int64 signal words

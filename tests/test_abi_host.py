@@ -120,3 +120,27 @@ def test_status_strings(lib):
     assert lib.llmoe_status_string(0) == "success"
     assert lib.llmoe_status_string(4) == "invalid argument"
     assert lib.llmoe_status_string(77) == "unknown status"
+
+
+def test_layout_bytes_dtype_matches_oracle(lib):
+    rnd = random.Random(7)
+    for _ in range(2000):
+        T, H, R, E = rnd.randint(1, 2048), rnd.randint(1, 8192), rnd.randint(1, 64), rnd.randint(1, 1024)
+        for code, es in ((0, 2), (1, 2), (2, 4)):
+            assert lib.llmoe_layout_bytes_dtype(T, H, R, E, code) == oracle.size_hint(T, H, R, E, es)
+    assert lib.llmoe_layout_bytes_dtype(8, 256, 2, 8, 3) == 0
+    assert lib.llmoe_layout_bytes_dtype(8, 256, 2, 8, -1) == 0
+    for code, es in ((0, 2), (1, 2), (2, 4)):
+        rc, L = oracle.layout(16, 96, 4, 32, es)
+        for s in (0, 1):
+            assert lib.llmoe_layout_offsets_dtype(16, 96, 4, 32, code, s) == (
+                L.dispatch_send[s], L.dispatch_recv[s], L.dispatch_recv_count[s])
+
+
+@pytest.mark.parametrize("kw", [dict(dtype=3), dict(dtype=-1), dict(dtype=2, hidden=6), dict(dtype=1, hidden=12),
+                                dict(dtype=2, hidden=2)])
+def test_invalid_dtype_rejected_before_launch(lib, kw):
+    bs = bs_for(lib, **kw)
+    A = 1 << 24
+    assert lib._lib.llmoe_dispatch(A, A, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT
+    assert lib._lib.llmoe_combine(A, A, A, 2 * A, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT

@@ -60,21 +60,34 @@ def all_equal_chunked(t: torch.Tensor, value: int, chunk=1 << 31) -> bool:
     return True
 
 
+def ulp_distance(got: np.ndarray, ref: np.ndarray, dtype: str) -> np.ndarray:
+    """Ordinal distance between the bit patterns of two float arrays."""
+    if dtype == "fp32":
+        g, r = got.view(np.uint32).astype(np.int64), ref.view(np.uint32).astype(np.int64)
+        og = np.where(g & 0x80000000, -(g & 0x7FFFFFFF), g)
+        orf = np.where(r & 0x80000000, -(r & 0x7FFFFFFF), r)
+        return np.abs(og - orf)
+    return np.abs(ordinal(got.view(np.uint16)) - ordinal(ref.view(np.uint16)))
+
+
 class Round:
     """One clean / dispatch / clean / combine round on fresh canary-filled buffers."""
 
-    def __init__(self, L, w: Workload, seed=0, tokens=None, dispatch_set=0, inp=None, validate=True):
-        self.L, self.w = L, w
-        self.inp = inp if inp is not None else make_inputs(w, seed=seed, tokens=tokens)
+    def __init__(self, L, w: Workload, seed=0, tokens=None, dispatch_set=0, inp=None, validate=True, dtype="bf16"):
+        self.L, self.w, self.dtype = L, w, dtype
+        self.inp = inp if inp is not None else make_inputs(w, seed=seed, tokens=tokens, dtype=dtype)
         self.T_call = self.inp["x"].shape[1]
-        self.rb = L.RankBuffers(w.T, w.H, w.R, w.E, guard=256, fill=CANARY)
+        self.rb = L.RankBuffers(w.T, w.H, w.R, w.E, guard=256, fill=CANARY, dtype=dtype)
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda") if validate else None
         self.ds, self.cs = dispatch_set, 1 - dispatch_set
         self.bs_d = self.rb.buf_set(self.ds, w.K, self.T_call, self.err)
         self.bs_c = self.rb.buf_set(self.cs, w.K, self.T_call, self.err)
         self.x, self.idx, self.wt = dev(self.inp["x"]), dev(self.inp["topk_idx"]), dev(self.inp["topk_w"])
         self.y = y_dev(self.inp)
-        self.out = torch.full((w.R, self.T_call, w.H), OUT_CANARY, dtype=torch.int16, device="cuda")
+        if dtype == "fp32":
+            self.out = torch.full((w.R, self.T_call, w.H), float("nan"), dtype=torch.float32, device="cuda")
+        else:
+            self.out = torch.full((w.R, self.T_call, w.H), OUT_CANARY, dtype=torch.int16, device="cuda")
 
     def run(self):
         L = self.L
@@ -91,10 +104,10 @@ class Round:
     def check_dispatch(self, d=None):
         w, inp = self.w, self.inp
         if d is None:
-            d = oracle.dispatch(inp["x"], inp["topk_idx"], w.E, num_max_tokens=w.T)
+            d = oracle.dispatch(inp["x"], inp["topk_idx"], w.E, num_max_tokens=w.T, dtype=self.dtype)
         recv = self.rb.recv_rows(self.ds)
         rr, ri = dev(d["row_rank"]), dev(d["row_index"])
-        got = recv[rr, ri].cpu().numpy() if d["n"] else np.zeros((0, 4 + 2 * w.H), np.uint8)
+        got = recv[rr, ri].cpu().numpy() if d["n"] else np.zeros((0, self.rb.msg_bytes), np.uint8)
         assert got.shape == d["msgs"].shape
         bad = np.nonzero((got != d["msgs"]).any(axis=1))[0]
         assert bad.size == 0, f"{bad.size} of {d['n']} messages differ; first at entry {bad[:5]}"
@@ -104,9 +117,8 @@ class Round:
     def check_combine(self):
         w, inp = self.w, self.inp
         ref, flags = oracle.combine((inp["y_pool"], inp["y_row_map"]), inp["topk_idx"], inp["topk_w"], w.H, w.E,
-                                    num_max_tokens=w.T)
-        got = self.out.cpu().numpy().view(np.uint16)
-        dist = np.abs(ordinal(got) - ordinal(ref))
+                                    num_max_tokens=w.T, dtype=self.dtype)
+        dist = ulp_distance(self.out.cpu().numpy(), ref, self.dtype)
         assert dist.max(initial=0) <= 1, f"max ulp distance {dist.max()}"
         assert int((dist != 0).sum()) == 0, f"{int((dist != 0).sum())} elements differ by 1 ulp"
         assert np.array_equal(self.rb.signal_words(self.cs).cpu().numpy(), flags)
@@ -446,14 +458,13 @@ def run_staged(L, r: Round):
     assert L.llmoe_get_error(r.bs_c) == 0
     w, inp = r.w, r.inp
     st = oracle.combine_staged((inp["y_pool"], inp["y_row_map"]), inp["topk_idx"], inp["topk_w"], w.H, w.E,
-                               num_max_tokens=w.T)
+                               num_max_tokens=w.T, dtype=r.dtype)
     recv = r.rb.recv_rows(r.cs)
     if st["n"]:
         got = recv[dev(st["msg_rank"]), dev(st["msg_row"])].cpu().numpy()
         bad = np.nonzero((got != st["msgs"]).any(axis=1))[0]
         assert bad.size == 0, f"{bad.size} of {st['n']} staged messages differ"
-    out = r.out.cpu().numpy().view(np.uint16)
-    dist = np.abs(ordinal(out) - ordinal(st["out"]))
+    dist = ulp_distance(r.out.cpu().numpy(), st["out"], r.dtype)
     assert dist.max(initial=0) <= 1 and int((dist != 0).sum()) == 0
     assert np.array_equal(r.rb.signal_words(r.cs).cpu().numpy(), st["flag_words"])
     # nothing but those messages and the signal words was written
@@ -493,3 +504,29 @@ def test_staged_equals_direct_on_gpu(L):
     L.llmoe_combine_staged(r.y, r.idx, r.wt, r.out, r.bs_c)
     torch.cuda.synchronize()
     assert torch.equal(direct, r.out)
+
+
+# ---------------------------------------------------------------------------
+# payload types other than bf16 (LLMoEBufferLayout<T>)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["fp16", "fp32"])
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed", "many_small"])
+def test_payload_types_round(L, name, dtype):
+    full_check(Round(L, WORKLOADS[name], seed=51, dtype=dtype))
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "fp32"])
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "skewed"])
+def test_payload_types_staged(L, name, dtype):
+    run_staged(L, Round(L, WORKLOADS[name], seed=52, dtype=dtype))
+
+
+@pytest.mark.parametrize("dtype,H", [("fp32", 4), ("fp32", 12), ("fp32", 36), ("fp16", 8), ("fp16", 56),
+                                     ("fp32", 2052)])
+@pytest.mark.parametrize("R,E,K,T", [(1, 8, 2, 3), (3, 15, 8, 37), (32, 32, 1, 3)])
+def test_payload_types_shapes(L, dtype, H, R, E, K, T):
+    w = Workload("typed", R, T, H, E, K, mask_p=0.3 if K > 1 else 0.0)
+    r = Round(L, w, seed=R + E + K + H + T, dtype=dtype)
+    full_check(r)
+    run_staged(L, Round(L, w, seed=R + E + K + H + T + 1, dtype=dtype))
