@@ -417,6 +417,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     timed = max_over_ranks([sum(step_ms), wall], world)
     round_us = timed[0] / args.steps * 1e3
 
+    pipe = run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream)
@@ -461,6 +463,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "gpu_launches": 2 * args.steps,
             "clocks": clocks.summary(),
         }
+        line["double_buffer"] = pipe
         if e2e is not None:
             line["e2e"] = e2e
         if not args.no_cpu_baseline:
@@ -469,6 +472,53 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es, micro_batches: int = 200):
+    """Micro-batches back to back: serial on one stream (clean, dispatch,
+    clean, combine on one set each) against the two-stream double-buffered
+    schedule, where micro-batch b+1's dispatch overlaps micro-batch b's
+    combine (sets b % 2).  No L2 flush between micro-batches: this is the
+    steady state of a pipeline."""
+    import torch
+
+    from combine_routing_count_prefix_gb300.pipeline import DoubleBufferPipeline
+
+    outs = [torch.empty((w.R, tokens, w.H), dtype=torch.float32 if es == 4 else torch.int16, device="cuda")
+            for _ in (0, 1)]
+    bs = [rb.buf_set(s, w.K) for s in (0, 1)]
+    cur = torch.cuda.current_stream()
+
+    def serial():
+        for b in range(micro_batches):
+            s = b % 2
+            llmoe.llmoe_clean(bs[s], cur)
+            llmoe.llmoe_dispatch(x, idx, bs[s], cur)
+            llmoe.llmoe_clean(bs[s], cur)
+            llmoe.llmoe_combine(y, idx, wt, outs[s], bs[s], cur)
+
+    pipe = DoubleBufferPipeline(rb, w.K)
+
+    def pipelined():
+        for b in range(micro_batches):
+            pipe.dispatch(b, x, idx)
+            pipe.combine(b, y, idx, wt, outs[b % 2])
+        pipe.join()
+
+    res = {}
+    for name, fn in (("serial", serial), ("pipelined", pipelined)):
+        fn()  # warm-up
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        fn()
+        b_.record(cur)
+        torch.cuda.synchronize()
+        res[f"{name}_us_per_microbatch"] = round(a.elapsed_time(b_) * 1e3 / micro_batches, 3)
+    res["micro_batches"] = micro_batches
+    res["note"] = ("micro-batch b uses buffer set b % 2; pipelined: dispatches on one stream, combines on another, "
+                   "b+1's dispatch overlapping b's combine; no L2 flush between micro-batches")
+    return res
 
 
 def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):

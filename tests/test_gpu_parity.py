@@ -530,3 +530,48 @@ def test_payload_types_shapes(L, dtype, H, R, E, K, T):
     r = Round(L, w, seed=R + E + K + H + T, dtype=dtype)
     full_check(r)
     run_staged(L, Round(L, w, seed=R + E + K + H + T + 1, dtype=dtype))
+
+
+# ---------------------------------------------------------------------------
+# two-stream double buffering: micro-batch b on set b % 2, b+1's dispatch
+# overlapping b's combine
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name,H", [("tiny", 256), ("skewed", 512), ("many_small", 256)])
+def test_double_buffer_pipeline(L, name, H):
+    from combine_routing_count_prefix_gb300.pipeline import DoubleBufferPipeline
+
+    w = WORKLOADS[name].with_(H=H)
+    M = 7
+    batches = [make_inputs(w, seed=60 + b) for b in range(M)]
+    rb = L.RankBuffers(w.T, w.H, w.R, w.E, guard=256, fill=CANARY)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pipe = DoubleBufferPipeline(rb, w.K, err=err)
+    dev_in = [(dev(b["x"]), dev(b["topk_idx"]), dev(b["topk_w"]), y_dev(b)) for b in batches]
+    outs = [torch.full((w.R, w.T, w.H), OUT_CANARY, dtype=torch.int16, device="cuda") for _ in range(M)]
+    snaps, flags = [None] * M, [None] * M
+    for b in range(M):
+        x, idx, wt, y = dev_in[b]
+        s = b % 2
+
+        def snap_dispatch(b=b, s=s):
+            snaps[b] = (rb.recv_rows(s).clone(), rb.signal_words(s).clone())
+
+        def snap_flags(b=b, s=s):
+            flags[b] = rb.signal_words(s).clone()
+
+        pipe.dispatch(b, x, idx, after=snap_dispatch)
+        pipe.combine(b, y, idx, wt, outs[b], after=snap_flags)
+    pipe.join()
+    torch.cuda.synchronize()
+    assert L.llmoe_get_error(pipe.bs[0]) == 0
+    for b in range(M):
+        inp = batches[b]
+        d = oracle.dispatch(inp["x"], inp["topk_idx"], w.E, num_max_tokens=w.T)
+        recv, counts = snaps[b]
+        got = recv[dev(d["row_rank"]), dev(d["row_index"])].cpu().numpy()
+        assert np.array_equal(got, d["msgs"]), f"micro-batch {b}: dispatch messages differ"
+        assert np.array_equal(counts.cpu().numpy(), d["count_words"])
+        ref, fl = oracle.combine((inp["y_pool"], inp["y_row_map"]), inp["topk_idx"], inp["topk_w"], w.H, w.E)
+        assert np.array_equal(outs[b].cpu().numpy().view(np.uint16), ref), f"micro-batch {b}: combine differs"
+        assert np.array_equal(flags[b].cpu().numpy(), fl)
