@@ -20,6 +20,8 @@ function follows:
 - ``combine_staged``: the combine through the combine receive buffers
   (LLMoEBuffer combine send / recv roles): messages [t | y row] at
   combine_recv[e][t] of the source rank, then the reduction from them.
+- ``unpack``: the received rows in the experts' input order (each local
+  expert's receive rows contiguous, the order the combine reads y in).
 - ``clean``: LLMoEBuffer::clean_meta.
 """
 from __future__ import annotations
@@ -113,6 +115,8 @@ def lib():
             L.oracle_combine.restype = i
             L.oracle_combine_staged.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P, P, P, P]
             L.oracle_combine_staged.restype = i
+            L.oracle_unpack.argtypes = [i, i, i, i, i, i, i, P, P, P, P, P, P]
+            L.oracle_unpack.restype = i
             L.oracle_clean.argtypes = [i, i, P]
             L.oracle_clean.restype = None
             _lib = L
@@ -294,6 +298,29 @@ def combine_staged(y_rows, topk_idx: np.ndarray, topk_w: np.ndarray, hidden: int
     n = n.value
     return {"msg_rank": msg_rank[:n], "msg_row": msg_row[:n], "msgs": msgs[:n], "out": out,
             "flag_words": flag_words, "n": n}
+
+
+def unpack(x: np.ndarray, topk_idx: np.ndarray, num_experts: int, num_max_tokens: int | None = None,
+           dtype: str = "bf16"):
+    """Expected unpack: dict with rows [n] (written rows of recv_x, in (src,
+    t, k) order), recv_x [E * R * T_max, H] (unwritten rows zero) and
+    recv_src int32 [E * R * T_max] (unwritten -1)."""
+    code, es, npdt = DTYPES[dtype]
+    x = np.ascontiguousarray(x, dtype=npdt)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    R, T, H = x.shape
+    K = idx.shape[2]
+    T_max = T if num_max_tokens is None else num_max_tokens
+    nrows = num_experts * R * T_max
+    recv_x = np.zeros((nrows, H), dtype=npdt)
+    recv_src = np.full(nrows, -1, dtype=np.int32)
+    rows = np.empty(max(R * T * K, 1), dtype=np.int64)
+    n = ctypes.c_int64(0)
+    rc = lib().oracle_unpack(R, T_max, T, H, num_experts, K, code, _ptr(x), _ptr(idx), _ptr(recv_x), _ptr(recv_src),
+                             _ptr(rows), ctypes.addressof(n))
+    if rc != OK:
+        raise OracleError(rc, "unpack")
+    return {"rows": rows[:n.value], "recv_x": recv_x, "recv_src": recv_src, "n": n.value}
 
 
 def clean(num_ranks: int, num_experts: int) -> np.ndarray:

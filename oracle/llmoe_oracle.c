@@ -538,3 +538,53 @@ int oracle_combine_staged(int R, int T_max, int T, int H, int E, int K, int dtyp
   free(slot); free(cnt); free(where); free(acc);
   return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Unpack: the received messages as the experts' input                      */
+/* ------------------------------------------------------------------------ */
+
+/* The experts' view of a dispatch: for every unmasked entry (src, t, k)
+ * choosing expert e, its token row x[src][t] at row e * R * T_max +
+ * src * T_max + slot of recv_x (for rank dst = e / L and local expert
+ * le = e % L that is recv_x[dst][le][src * T_max + slot]: the receive rows
+ * of each local expert laid out contiguously, the same order the combine
+ * reads its expert outputs in), and the token index t at the same position
+ * of recv_src.  Rows no entry reaches are not written.  Returns the number of
+ * rows written in *n_out and, in rows[n], which rows they are, in (src, t, k)
+ * order. */
+int oracle_unpack(int R, int T_max, int T, int H, int E, int K, int dtype, const uint8_t* x, const int64_t* idx,
+                  uint8_t* recv_x, int32_t* recv_src, int64_t* rows, int64_t* n_out) {
+  *n_out = 0;
+  if (R < 1 || T_max < 1 || T < 0 || T > T_max || H < 1 || E < 1 || K < 1 || E % R != 0) return ORACLE_BAD_ARG;
+  int64_t ntk = (int64_t)R * T * K;
+  int32_t* slot = (int32_t*)malloc((size_t)(ntk > 0 ? ntk : 1) * sizeof(int32_t));
+  int64_t* cnt = (int64_t*)malloc((size_t)E * R * sizeof(int64_t));
+  if (!slot || !cnt) {
+    free(slot);
+    free(cnt);
+    return ORACLE_BAD_ARG;
+  }
+  int rc = oracle_route(R, T, K, E, idx, slot, cnt);
+  if (rc != ORACLE_OK) {
+    free(slot);
+    free(cnt);
+    return rc;
+  }
+  const size_t row_bytes = (size_t)H * elem_size(dtype);
+  int64_t n = 0;
+  for (int src = 0; src < R; ++src)
+    for (int t = 0; t < T; ++t)
+      for (int k = 0; k < K; ++k) {
+        int64_t pos = ((int64_t)src * T + t) * K + k;
+        int64_t e = idx[pos];
+        if (e < 0) continue;
+        int64_t row = e * R * T_max + (int64_t)src * T_max + slot[pos];
+        memcpy(recv_x + (size_t)row * row_bytes, x + ((size_t)src * T + t) * row_bytes, row_bytes);
+        recv_src[row] = t;
+        rows[n++] = row;
+      }
+  *n_out = n;
+  free(slot);
+  free(cnt);
+  return ORACLE_OK;
+}
