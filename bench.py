@@ -418,6 +418,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     round_us = timed[0] / args.steps * 1e3
 
     pipe = run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es)
+    signaled = run_signaled(args, llmoe, w, x, idx, rb, es, flush)
 
     e2e = None
     if not args.no_e2e:
@@ -464,6 +465,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "clocks": clocks.summary(),
         }
         line["double_buffer"] = pipe
+        line["dispatch_unpack"] = signaled
         if e2e is not None:
             line["e2e"] = e2e
         if not args.no_cpu_baseline:
@@ -518,6 +520,46 @@ def run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es, micro_batches: i
     res["micro_batches"] = micro_batches
     res["note"] = ("micro-batch b uses buffer set b % 2; pipelined: dispatches on one stream, combines on another, "
                    "b+1's dispatch overlapping b's combine; no L2 flush between micro-batches")
+    return res
+
+
+def run_signaled(args, llmoe, w, x, idx, rb, es, flush, steps: int = 200):
+    """Dispatch plus unpack (received rows in the experts' input order): two
+    launches (llmoe_dispatch, llmoe_unpack) against one cooperative launch
+    whose CTAs signal each other through the count words
+    (llmoe_dispatch_signaled, bounded waits).  L2 flushed before each."""
+    import torch
+
+    rows = w.E * w.R * w.T
+    recv_x = torch.empty((rows, w.H), dtype=torch.float32 if es == 4 else torch.int16, device="cuda")
+    recv_src = torch.empty((rows,), dtype=torch.int32, device="cuda")
+    bs = rb.buf_set(0, w.K)
+    ws = torch.zeros(llmoe.llmoe_signal_workspace_bytes(bs) // 4, dtype=torch.int32, device="cuda")
+    cur = torch.cuda.current_stream()
+
+    def two_launches():
+        llmoe.llmoe_dispatch(x, idx, bs, cur)
+        llmoe.llmoe_unpack(recv_x, recv_src, bs, cur)
+
+    def one_launch():
+        llmoe.llmoe_dispatch_signaled(x, idx, recv_x, recv_src, ws, 2_000_000_000, bs, cur)
+
+    res = {}
+    for name, fn in (("dispatch_then_unpack_us", two_launches), ("signaled_us", one_launch)):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps + 3):
+            flush()
+            llmoe.llmoe_clean(bs, cur)
+            if i >= 3:
+                evs[i - 3][0].record(cur)
+            fn()
+            if i >= 3:
+                evs[i - 3][1].record(cur)
+        torch.cuda.synchronize()
+        res[name] = round(statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3, 3)
+    res["steps"] = steps
+    res["note"] = ("events around the dispatch (+ unpack) only; the clean before each is outside; "
+                   "signaled: one cooperative launch, consumers wait on the count words with a clock limit")
     return res
 
 

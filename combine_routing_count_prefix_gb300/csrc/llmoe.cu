@@ -743,6 +743,183 @@ __global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, co
   }
 }
 
+// ---------------------------------------------------------------------------
+// unpack, and the dispatch whose CTAs signal each other
+// ---------------------------------------------------------------------------
+
+// Unpacks one bucket (expert e, source src): its `cnt` messages, starting at
+// `msg0` (slot 0), into the rows starting at `row0`, headers into src0.  The
+// CTA's warps take (slot, chunk) units, four at a time so that each lane has
+// four loads in flight before it shuffles and stores.
+constexpr int kUnpackBatch = 4;
+
+__device__ __forceinline__ void unpack_bucket(const Geometry& g, const uint8_t* msg0, uint8_t* row0,
+                                              int32_t* src0, int cnt, bool l2_only) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int n = cnt * g.nchunks;
+  for (int r0 = warp; r0 < n; r0 += kUnpackBatch * nwarps) {
+    uint4 a[kUnpackBatch], t[kUnpackBatch];
+#pragma unroll
+    for (int i = 0; i < kUnpackBatch; ++i) {
+      const int r = r0 + i * nwarps;
+      a[i] = t[i] = make_uint4(0, 0, 0, 0);
+      if (r < n) {
+        const int slot = r / g.nchunks, c = r % g.nchunks, j = c * 32 + lane;
+        const uintptr_t pa = reinterpret_cast<uintptr_t>(msg0 + (size_t)slot * g.msg) + 4;
+        const int phase = (int)((pa >> 2) & 3);
+        const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
+        if (j < g.nq || (j == g.nq && phase != 0)) a[i] = l2_only ? __ldcg(qb + j) : __ldg(qb + j);
+        if (lane == 31 && phase != 0 && j < g.nq) t[i] = l2_only ? __ldcg(qb + j + 1) : __ldg(qb + j + 1);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kUnpackBatch; ++i) {
+      const int r = r0 + i * nwarps;
+      if (r >= n) break;  // the whole warp
+      const int slot = r / g.nchunks, c = r % g.nchunks, j = c * 32 + lane;
+      const uint8_t* msg = msg0 + (size_t)slot * g.msg;
+      const int phase = (int)(((reinterpret_cast<uintptr_t>(msg) + 4) >> 2) & 3);
+      uint4 b = shfl_down16(a[i]);
+      if (lane == 31) b = t[i];
+      if (j < g.nq) reinterpret_cast<uint4*>(row0 + (size_t)slot * g.row_bytes)[j] = unshift_words(a[i], b, phase);
+      if (c == 0 && lane == 0)
+        src0[slot] = l2_only ? __ldcg(reinterpret_cast<const int32_t*>(msg)) : *reinterpret_cast<const int32_t*>(msg);
+    }
+  }
+}
+
+// Unpack after a dispatch: CTA per bucket (expert e, source src), grid-stride;
+// the bucket's count word gives how many of its slots hold a message.
+__global__ void __launch_bounds__(kThreads) unpack_kernel(Geometry g, void* __restrict__ recv_x,
+                                                          int32_t* __restrict__ recv_src) {
+  release_next_grid();
+  wait_prior_grid();
+  const int64_t nbuckets = (int64_t)g.E * g.R;
+  for (int64_t bucket = blockIdx.x; bucket < nbuckets; bucket += gridDim.x) {
+    const int e = (int)(bucket / g.R), src = (int)(bucket % g.R), dst = e / g.L, le = e % g.L;
+    const uint8_t* rank = g.base + dst * g.rank_stride;
+    const int64_t c64 = reinterpret_cast<const int64_t*>(rank + g.sig_off)[(int64_t)le * g.R + src];
+    const int cnt = (int)max((int64_t)0, min(c64, (int64_t)g.T_max));
+    const uint8_t* msg0 = rank + g.recv_off + ((uint64_t)le * g.R + src) * g.T_max * g.msg;
+    uint8_t* row0 = reinterpret_cast<uint8_t*>(recv_x) + bucket * g.T_max * g.row_bytes;
+    unpack_bucket(g, msg0, row0, recv_src + bucket * g.T_max, cnt, false);
+  }
+}
+
+__device__ __forceinline__ long long ld_acquire_gpu(const long long* p) {
+  long long v;
+  asm volatile("ld.acquire.gpu.global.s64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(long long* p, long long v) {
+  asm volatile("st.release.gpu.global.s64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Cooperative: every CTA is resident, so a consumer that waits on a signal
+// word only waits for producers that are running.  Producer work (CTA =
+// source rank src, token block) is the dispatch; the CTA that completes a
+// source (per-source counter in `done`) raises its signal words as
+// -(count + 1).  Consumer work takes buckets (expert e, source src) round
+// robin, waits (bounded) for the bucket's word, unpacks its rows and rewrites
+// the word to the plain count.
+__global__ void __launch_bounds__(kThreads) dispatch_signaled_kernel(Geometry g, const void* __restrict__ x,
+                                                                     const int64_t* __restrict__ idx,
+                                                                     void* __restrict__ recv_x,
+                                                                     int32_t* __restrict__ recv_src,
+                                                                     int32_t* __restrict__ done, long long spin_limit) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const RouteSmem s = carve_route(smem, g);
+  uintptr_t* s_dst = reinterpret_cast<uintptr_t*>(s.slot + g.TB * g.K + (g.E & 1));
+  __shared__ int s_last;
+  __shared__ long long s_word;
+
+  const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
+  const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
+  const int nblock = (t1 - t0) * g.K;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- producer: this CTA's rows
+  route_hist(g, idx, src, t0, t1, s);
+  for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
+    const int e = s.ent[q], sl = route_slot(g, s, q);
+    uintptr_t d = 0;
+    if (sl >= 0) {
+      const int dst = e / g.L, le = e % g.L;
+      const uint64_t row = ((uint64_t)le * g.R + src) * g.T_max + sl;
+      d = pack_dest(g.base + dst * g.rank_stride + g.recv_off + row * g.msg);
+    }
+    s_dst[q] = d;
+  }
+  __syncthreads();
+  const int nunits = (t1 - t0) * g.nchunks;
+  for (int u = warp; u < nunits; u += kThreads / 32) {
+    const int tl = u / g.nchunks, c = u % g.nchunks, t = t0 + tl, j = c * 32 + lane;
+    const uint4* xrow =
+        reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(x) + ((int64_t)src * g.T + t) * g.row_bytes);
+    const uint4 cur = j < g.nq ? __ldg(xrow + j) : make_uint4(0, 0, 0, 0);
+    uint4 prev = shfl_up16(cur);
+    if (lane == 0) prev = j == 0 ? make_uint4(0, 0, 0, (uint32_t)t) : __ldg(xrow + j - 1);
+    if (j < g.nq)
+      for (int k = 0; k < g.K; ++k) {
+        const uintptr_t d = s_dst[tl * g.K + k];
+        if (d != 0) put_quad(d, j, g.nq, prev, cur);
+      }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's rows before its completion count
+    s_last = atomicAdd(&done[src], 1) == g.nblk - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    // every CTA of src has written its rows: raise src's signal words
+    __threadfence();
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) s.hist[e] = 0;
+    __syncthreads();
+    const int64_t* src_idx = idx + (int64_t)src * g.T * g.K;
+    for (int i = threadIdx.x; i < g.T * g.K; i += blockDim.x) {
+      const int64_t e = src_idx[i];
+      if (e >= 0 && e < g.E) atomicAdd(&s.hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+      long long* w = reinterpret_cast<long long*>(g.base + (e / g.L) * g.rank_stride + g.sig_off) +
+                     ((int64_t)(e % g.L) * g.R + src);
+      if (g.err != nullptr && *reinterpret_cast<volatile long long*>(w) != 0) report(g.err, LLMOE_DEV_STALE_SIGNAL);
+      st_release_gpu(w, -(long long)s.hist[e] - 1);
+    }
+    if (threadIdx.x == 0) done[src] = 0;  // ready for the next call
+  }
+
+  // ---- consumer: buckets (e, bsrc), round robin over the CTAs
+  const int64_t nbuckets = (int64_t)g.E * g.R;
+  for (int64_t bucket = blockIdx.x; bucket < nbuckets; bucket += gridDim.x) {
+    const int e = (int)(bucket / g.R), bsrc = (int)(bucket % g.R), dst = e / g.L, le = e % g.L;
+    uint8_t* rank = g.base + dst * g.rank_stride;
+    long long* word = reinterpret_cast<long long*>(rank + g.sig_off) + ((int64_t)le * g.R + bsrc);
+    __syncthreads();  // s_word of the previous bucket has been read
+    if (threadIdx.x == 0) {
+      long long v = ld_acquire_gpu(word);
+      const long long start = clock64();
+      while (v == 0 && clock64() - start <= spin_limit) {
+        __nanosleep(64);
+        v = ld_acquire_gpu(word);
+      }
+      if (v == 0) report(g.err, LLMOE_DEV_TIMEOUT);
+      s_word = v;
+    }
+    __syncthreads();
+    const long long v = s_word;
+    if (v >= 0) continue;  // timed out (0), or not a raised signal: leave the bucket
+    const int cnt = (int)min(-v - 1, (long long)g.T_max);
+    unpack_bucket(g, rank + g.recv_off + ((uint64_t)le * g.R + bsrc) * g.T_max * g.msg,
+                  reinterpret_cast<uint8_t*>(recv_x) + bucket * g.T_max * g.row_bytes, recv_src + bucket * g.T_max,
+                  cnt, true);
+    __syncthreads();
+    if (threadIdx.x == 0) *word = -v - 1;  // the plain count, as a dispatch leaves it
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) route_kernel(Geometry g, const int64_t* __restrict__ idx,
                                                          int32_t* __restrict__ slot_out,
                                                          int64_t* __restrict__ counts) {
@@ -914,7 +1091,9 @@ enum KernelId {
   kCombineKernel = 2,
   kCombinePutKernel = 3,
   kCombineReduceKernel = 4,
-  kNumKernels = 5
+  kUnpackKernel = 5,
+  kSignaledKernel = 6,
+  kNumKernels = 7
 };
 int g_occupancy[64][32] = {{0}};
 
@@ -1099,6 +1278,64 @@ int llmoe_combine_staged(const void* y, const int64_t* topk_idx, const float* to
     case LLMOE_DTYPE_FP32: return launch_reduce<LLMOE_DTYPE_FP32>(gr, topk_idx, topk_w, out, stream);
     default: return launch_reduce<LLMOE_DTYPE_BF16>(gr, topk_idx, topk_w, out, stream);
   }
+}
+
+int llmoe_unpack(void* recv_x, int32_t* recv_src, const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
+  Geometry g;
+  int rc = make_geometry(bs, true, &g);
+  if (rc != LLMOE_SUCCESS) return rc;
+  if (recv_x == nullptr || recv_src == nullptr || !aligned(recv_x, 16) || !aligned(recv_src, 4))
+    return LLMOE_ERR_INVALID_ARGUMENT;
+  const int64_t wave =
+      (int64_t)num_sms() * blocks_per_sm(kslot(kUnpackKernel), (const void*)unpack_kernel, kThreads, 0);
+  const int64_t blocks = std::min<int64_t>(wave, (int64_t)g.E * g.R);
+  return launch(unpack_kernel, (unsigned)blocks, kThreads, 0, stream, g, recv_x, recv_src);
+}
+
+size_t llmoe_signal_workspace_bytes(const llmoe_buf_set_t* bs) {
+  if (bs == nullptr || bs->num_ranks < 1) return 0;
+  return ((size_t)bs->num_ranks * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src, void* workspace,
+                            int64_t spin_limit, const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
+  Geometry g;
+  int rc = make_geometry(bs, true, &g);
+  if (rc != LLMOE_SUCCESS) return rc;
+  if ((g.T > 0 && (x == nullptr || topk_idx == nullptr || !aligned(x, 16) || !aligned(topk_idx, 8))) ||
+      recv_x == nullptr || recv_src == nullptr || !aligned(recv_x, 16) || !aligned(recv_src, 4) ||
+      workspace == nullptr || !aligned(workspace, 4) || spin_limit < 1)
+    return LLMOE_ERR_INVALID_ARGUMENT;
+  const size_t smem_one = route_smem_bytes(g) + sizeof(uintptr_t) * (size_t)g.K;
+  const int occ = blocks_per_sm(kslot(kSignaledKernel), (const void*)dispatch_signaled_kernel, kThreads, smem_one);
+  set_blocking(&g, occ);
+  const size_t smem = route_smem_bytes(g) + sizeof(uintptr_t) * (size_t)g.TB * g.K;
+  if ((rc = set_smem(kslot(kSignaledKernel), (const void*)dispatch_signaled_kernel, smem)) != LLMOE_SUCCESS)
+    return rc;
+  int fit = 0;  // the exact smem of this launch may lower the occupancy
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, (const void*)dispatch_signaled_kernel, kThreads, smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return LLMOE_ERR_CUDA;
+  }
+  const int64_t grid = (int64_t)g.R * g.nblk;
+  if (grid > (int64_t)num_sms() * fit) return LLMOE_ERR_INVALID_ARGUMENT;  // not all CTAs could be resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, dispatch_signaled_kernel, g, x, topk_idx, recv_x, recv_src,
+                         static_cast<int32_t*>(workspace), (long long)spin_limit) != cudaSuccess) {
+    cudaGetLastError();
+    return LLMOE_ERR_CUDA;
+  }
+  return LLMOE_SUCCESS;
 }
 
 int llmoe_clean(const llmoe_buf_set_t* bs, llmoe_stream_t stream) {

@@ -42,7 +42,8 @@ LLMOE_MAX_TOPK = 32
 LLMOE_MAX_EXPERTS = 8192
 
 EXPORTS = ("llmoe_layout_bytes", "llmoe_layout_bytes_dtype", "llmoe_layout_offsets", "llmoe_layout_offsets_dtype",
-           "llmoe_route", "llmoe_dispatch", "llmoe_combine", "llmoe_combine_staged", "llmoe_clean", "llmoe_get_error",
+           "llmoe_route", "llmoe_dispatch", "llmoe_combine", "llmoe_combine_staged", "llmoe_unpack",
+           "llmoe_signal_workspace_bytes", "llmoe_dispatch_signaled", "llmoe_clean", "llmoe_get_error",
            "llmoe_status_string")
 
 LLMOE_DTYPE_BF16, LLMOE_DTYPE_FP16, LLMOE_DTYPE_FP32 = 0, 1, 2
@@ -86,6 +87,12 @@ _lib.llmoe_combine.argtypes = [_P, _P, _P, _P, _BS, _P]
 _lib.llmoe_combine.restype = _I
 _lib.llmoe_combine_staged.argtypes = [_P, _P, _P, _P, _BS, _P]
 _lib.llmoe_combine_staged.restype = _I
+_lib.llmoe_unpack.argtypes = [_P, _P, _BS, _P]
+_lib.llmoe_unpack.restype = _I
+_lib.llmoe_signal_workspace_bytes.argtypes = [_BS]
+_lib.llmoe_signal_workspace_bytes.restype = ctypes.c_size_t
+_lib.llmoe_dispatch_signaled.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int64, _BS, _P]
+_lib.llmoe_dispatch_signaled.restype = _I
 _lib.llmoe_clean.argtypes = [_BS, _P]
 _lib.llmoe_clean.restype = _I
 _lib.llmoe_get_error.argtypes = [_BS, _P, ctypes.POINTER(ctypes.c_int32), _I]
@@ -185,6 +192,22 @@ def llmoe_combine(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=None) ->
 def llmoe_combine_staged(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=None) -> None:
     _check(_lib.llmoe_combine_staged(_addr(y, "payload"), _addr(topk_idx, "i64"), _addr(topk_w, "f32"),
                                      _addr(out, "payload"), ctypes.byref(bs), _stream(stream)), "llmoe_combine_staged")
+
+
+def llmoe_unpack(recv_x, recv_src, bs: llmoe_buf_set_t, stream=None) -> None:
+    _check(_lib.llmoe_unpack(_addr(recv_x, "payload"), _addr(recv_src, "i32"), ctypes.byref(bs), _stream(stream)),
+           "llmoe_unpack")
+
+
+def llmoe_signal_workspace_bytes(bs: llmoe_buf_set_t) -> int:
+    return int(_lib.llmoe_signal_workspace_bytes(ctypes.byref(bs)))
+
+
+def llmoe_dispatch_signaled(x, topk_idx, recv_x, recv_src, workspace, spin_limit: int, bs: llmoe_buf_set_t,
+                            stream=None) -> None:
+    _check(_lib.llmoe_dispatch_signaled(_addr(x, "payload"), _addr(topk_idx, "i64"), _addr(recv_x, "payload"),
+                                        _addr(recv_src, "i32"), _addr(workspace, "i32"), int(spin_limit),
+                                        ctypes.byref(bs), _stream(stream)), "llmoe_dispatch_signaled")
 
 
 def llmoe_clean(bs: llmoe_buf_set_t, stream=None) -> None:

@@ -223,6 +223,47 @@ LLMOE_API int llmoe_combine(const void* y, const int64_t* topk_idx, const float*
 LLMOE_API int llmoe_combine_staged(const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                                    const llmoe_buf_set_t* bs, llmoe_stream_t stream);
 
+/* Unpack: the experts' view of a completed dispatch on set `set`.  For every
+ * rank dst, local expert le and source rank src, reads the bucket's count
+ * (rank dst's signal word le * R + src) and its messages
+ * recv[le][src][0..count), and writes each message's payload to row
+ * (dst * L + le) * R * T + src * T + slot of recv_x and its header (the source
+ * token index) to the same position of recv_src.  recv_x [E * R * T][H] of the
+ * payload type (16-byte aligned) thus holds each local expert's received rows
+ * contiguously, in the order llmoe_combine reads its expert outputs y;
+ * recv_src is int32 [E * R * T].  Rows past a bucket's count are not written.
+ * Uses no routing input: the counts in the rank buffers drive it. */
+LLMOE_API int llmoe_unpack(void* recv_x, int32_t* recv_src, const llmoe_buf_set_t* bs, llmoe_stream_t stream);
+
+/* Bytes of the workspace llmoe_dispatch_signaled needs for this geometry.
+ * No counterpart in the layout header: it holds one completion counter per
+ * source rank. */
+LLMOE_API size_t llmoe_signal_workspace_bytes(const llmoe_buf_set_t* bs);
+
+/* Dispatch and unpack in one cooperative launch whose CTAs signal each other
+ * through the recv-count words, the way the expert-parallel exchange signals
+ * a receiving rank (one-sided put, then signal; the receiver reads only after
+ * its wait returns: mscclpp.h, mscclppDevConn put / signal / wait).
+ * Producer work is the dispatch of llmoe_dispatch.  When every CTA of a
+ * source rank has written its rows, the last one writes that source's
+ * signal words as -(count + 1).  Consumer work (the buckets of every
+ * destination rank, spread over the same CTAs) waits for each bucket's signal
+ * word to become non-zero, then unpacks it as llmoe_unpack does and rewrites
+ * the word to the plain count.  The result is that of llmoe_dispatch followed
+ * by llmoe_unpack.
+ *   workspace   device memory of llmoe_signal_workspace_bytes(bs) bytes,
+ *               zero before the first call; each completed call leaves it
+ *               zero.  After an LLMOE_DEV_TIMEOUT, zero it again.
+ *   spin_limit  clock cycles a consumer waits for one signal word before it
+ *               records LLMOE_DEV_TIMEOUT (needs bs->err) and skips that
+ *               bucket; about 2e9 is one second at 2 GHz.  Unlike the
+ *               unbounded waits of mscclpp.h, no wait here can hang.
+ * Returns LLMOE_ERR_INVALID_ARGUMENT when the grid this geometry needs cannot
+ * be resident all at once (the signalling needs every CTA running). */
+LLMOE_API int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src,
+                                      void* workspace, int64_t spin_limit, const llmoe_buf_set_t* bs,
+                                      llmoe_stream_t stream);
+
 /* Clean (LLMoEBuffer::clean_meta): zero the num_experts int64 signal words
  * of buffer set `set` in each of the R rank buffers.  This resets both the
  * dispatch recv counts and the combine recv flags, which share the words. */

@@ -575,3 +575,103 @@ def test_double_buffer_pipeline(L, name, H):
         ref, fl = oracle.combine((inp["y_pool"], inp["y_row_map"]), inp["topk_idx"], inp["topk_w"], w.H, w.E)
         assert np.array_equal(outs[b].cpu().numpy().view(np.uint16), ref), f"micro-batch {b}: combine differs"
         assert np.array_equal(flags[b].cpu().numpy(), fl)
+
+
+# ---------------------------------------------------------------------------
+# unpack, and the dispatch whose CTAs signal each other (bounded waits)
+# ---------------------------------------------------------------------------
+
+def unpack_buffers(w, dtype="bf16"):
+    rows = w.E * w.R * w.T
+    if dtype == "fp32":
+        recv_x = torch.full((rows, w.H), float("nan"), dtype=torch.float32, device="cuda")
+    else:
+        recv_x = torch.full((rows, w.H), OUT_CANARY, dtype=torch.int16, device="cuda")
+    recv_src = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
+    return recv_x, recv_src
+
+
+def check_unpack(r: Round, recv_x, recv_src):
+    w, inp = r.w, r.inp
+    u = oracle.unpack(inp["x"], inp["topk_idx"], w.E, num_max_tokens=w.T, dtype=r.dtype)
+    got_x = recv_x.cpu().numpy()
+    got_src = recv_src.cpu().numpy()
+    rows = u["rows"]
+    assert np.array_equal(got_x[rows].view(np.uint8), u["recv_x"][rows].view(np.uint8))
+    assert np.array_equal(got_src[rows], u["recv_src"][rows])
+    untouched = np.ones(got_src.shape[0], dtype=bool)
+    untouched[rows] = False
+    assert (got_src[untouched] == -7).all()
+    if r.dtype == "fp32":
+        assert np.isnan(got_x[untouched]).all()
+    else:
+        assert (got_x[untouched].view(np.uint16) == OUT_CANARY).all()
+
+
+@pytest.mark.parametrize("name,dtype", [("tiny", "bf16"), ("dsv3", "bf16"), ("skewed", "bf16"), ("many_small", "bf16"),
+                                        ("skewed", "fp32"), ("many_small", "fp16")])
+def test_unpack_after_dispatch(L, name, dtype):
+    w = WORKLOADS[name]
+    r = Round(L, w, seed=81, dtype=dtype)
+    recv_x, recv_src = unpack_buffers(w, dtype)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch(r.x, r.idx, r.bs_d)
+    L.llmoe_unpack(recv_x, recv_src, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    r.check_dispatch()
+    check_unpack(r, recv_x, recv_src)
+
+
+@pytest.mark.parametrize("name,dtype", [("tiny", "bf16"), ("dsv3", "bf16"), ("skewed", "bf16"), ("many_small", "bf16"),
+                                        ("skewed", "fp32"), ("large", "bf16")])
+def test_dispatch_signaled(L, name, dtype):
+    w = WORKLOADS[name]
+    r = Round(L, w, seed=82, dtype=dtype)
+    recv_x, recv_src = unpack_buffers(w, dtype)
+    ws = torch.zeros(L.llmoe_signal_workspace_bytes(r.bs_d) // 4, dtype=torch.int32, device="cuda")
+    for rep in range(3):
+        L.llmoe_clean(r.bs_d)
+        L.llmoe_dispatch_signaled(r.x, r.idx, recv_x, recv_src, ws, 2_000_000_000, r.bs_d)
+        torch.cuda.synchronize()
+        assert r.error() == 0
+        assert not ws.any(), "the workspace is left zero"
+        d = r.check_dispatch()  # messages and plain counts, as llmoe_dispatch leaves them
+        check_unpack(r, recv_x, recv_src)
+    r.check_canary(d)
+
+
+def test_dispatch_signaled_times_out_without_signals(L):
+    # completion counters that never reach the last CTA: no source ever
+    # raises its signal words, so every consumer wait runs out
+    w = WORKLOADS["tiny"]
+    r = Round(L, w, seed=83)
+    recv_x, recv_src = unpack_buffers(w)
+    ws = torch.full((L.llmoe_signal_workspace_bytes(r.bs_d) // 4,), 1 << 30, dtype=torch.int32, device="cuda")
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch_signaled(r.x, r.idx, recv_x, recv_src, ws, 200_000, r.bs_d)
+    torch.cuda.synchronize()
+    assert L.llmoe_get_error(r.bs_d, reset=True) == L.LLMOE_DEV_TIMEOUT
+    assert (recv_src == -7).all(), "no bucket is unpacked without its signal"
+    # zeroed again, the same buffers work
+    ws.zero_()
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch_signaled(r.x, r.idx, recv_x, recv_src, ws, 2_000_000_000, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    r.check_dispatch()
+    check_unpack(r, recv_x, recv_src)
+
+
+def test_dispatch_signaled_refuses_a_grid_that_cannot_be_resident(L):
+    w = Workload("wide", 8, 100_000, 8, 8, 1)
+    rb = L.RankBuffers(w.T, w.H, w.R, w.E)
+    bs = rb.buf_set(0, w.K)
+    x = torch.zeros((w.R, w.T, w.H), dtype=torch.int16, device="cuda")
+    idx = torch.zeros((w.R, w.T, w.K), dtype=torch.int64, device="cuda")
+    recv_x = torch.zeros((w.E * w.R * w.T, w.H), dtype=torch.int16, device="cuda")
+    recv_src = torch.zeros((w.E * w.R * w.T,), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(64, dtype=torch.int32, device="cuda")
+    with pytest.raises(L.LLMoEError) as ei:
+        L.llmoe_dispatch_signaled(x, idx, recv_x, recv_src, ws, 1000, bs)
+    assert ei.value.status == L.LLMOE_ERR_INVALID_ARGUMENT
