@@ -1151,6 +1151,37 @@ int launch(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
   return LLMOE_SUCCESS;
 }
 
+// Workspace of llmoe_dispatch_signaled_static: the per-source completion
+// counters live in this fixed device array instead of memory the caller
+// allocates.  Every GPU that loads the library holds it until the process
+// exits; every call on a device shares it.
+constexpr int kStaticMaxRanks = LLMOE_STATIC_MAX_RANKS;
+static __device__ __align__(256) int32_t g_static_counters[kStaticMaxRanks];
+
+// The array's device address, looked up once per device (with that device
+// current): host code must not hand the symbol itself to a kernel.
+int32_t* g_static_counters_addr[64] = {nullptr};
+
+int static_counters(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return LLMOE_ERR_CUDA;
+  }
+  if (dev < 64 && g_static_counters_addr[dev] != nullptr) {
+    *out = g_static_counters_addr[dev];
+    return LLMOE_SUCCESS;
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_counters) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return LLMOE_ERR_CUDA;
+  }
+  if (dev < 64) g_static_counters_addr[dev] = static_cast<int32_t*>(p);
+  *out = static_cast<int32_t*>(p);
+  return LLMOE_SUCCESS;
+}
+
 template <int DT>
 int launch_combine(Geometry& g, const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                    llmoe_stream_t stream) {
@@ -1336,6 +1367,22 @@ int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, void* recv_x
     return LLMOE_ERR_CUDA;
   }
   return LLMOE_SUCCESS;
+}
+
+int llmoe_dispatch_signaled_static(const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src,
+                                   int64_t spin_limit, const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
+  if (bs == nullptr || bs->num_ranks < 1) return LLMOE_ERR_INVALID_ARGUMENT;
+  if (bs->num_ranks > kStaticMaxRanks) return LLMOE_ERR_INVALID_ARGUMENT;  // more ranks than the array holds
+  int32_t* counters = nullptr;
+  int rc = static_counters(&counters);
+  if (rc != LLMOE_SUCCESS) return rc;
+  // the counters must start at zero; a previous call may have left them
+  // otherwise (a timeout), so clear the part this call uses, in stream order
+  if (cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)bs->num_ranks, (cudaStream_t)stream) != cudaSuccess) {
+    cudaGetLastError();
+    return LLMOE_ERR_CUDA;
+  }
+  return llmoe_dispatch_signaled(x, topk_idx, recv_x, recv_src, counters, spin_limit, bs, stream);
 }
 
 int llmoe_clean(const llmoe_buf_set_t* bs, llmoe_stream_t stream) {

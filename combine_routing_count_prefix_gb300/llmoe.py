@@ -38,12 +38,15 @@ LLMOE_DEV_BAD_MESSAGE = 6
 LLMOE_FLAG_INPUTS_READY = 1
 LLMOE_FLAG_CLEAN_OTHER_SET = 2
 
+LLMOE_STATIC_MAX_RANKS = 1024
+
 LLMOE_MAX_TOPK = 32
 LLMOE_MAX_EXPERTS = 8192
 
 EXPORTS = ("llmoe_layout_bytes", "llmoe_layout_bytes_dtype", "llmoe_layout_offsets", "llmoe_layout_offsets_dtype",
            "llmoe_route", "llmoe_dispatch", "llmoe_combine", "llmoe_combine_staged", "llmoe_unpack",
-           "llmoe_signal_workspace_bytes", "llmoe_dispatch_signaled", "llmoe_clean", "llmoe_get_error",
+           "llmoe_signal_workspace_bytes", "llmoe_dispatch_signaled", "llmoe_dispatch_signaled_static", "llmoe_clean",
+           "llmoe_get_error",
            "llmoe_status_string")
 
 LLMOE_DTYPE_BF16, LLMOE_DTYPE_FP16, LLMOE_DTYPE_FP32 = 0, 1, 2
@@ -93,6 +96,8 @@ _lib.llmoe_signal_workspace_bytes.argtypes = [_BS]
 _lib.llmoe_signal_workspace_bytes.restype = ctypes.c_size_t
 _lib.llmoe_dispatch_signaled.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int64, _BS, _P]
 _lib.llmoe_dispatch_signaled.restype = _I
+_lib.llmoe_dispatch_signaled_static.argtypes = [_P, _P, _P, _P, ctypes.c_int64, _BS, _P]
+_lib.llmoe_dispatch_signaled_static.restype = _I
 _lib.llmoe_clean.argtypes = [_BS, _P]
 _lib.llmoe_clean.restype = _I
 _lib.llmoe_get_error.argtypes = [_BS, _P, ctypes.POINTER(ctypes.c_int32), _I]
@@ -208,6 +213,16 @@ def llmoe_dispatch_signaled(x, topk_idx, recv_x, recv_src, workspace, spin_limit
     _check(_lib.llmoe_dispatch_signaled(_addr(x, "payload"), _addr(topk_idx, "i64"), _addr(recv_x, "payload"),
                                         _addr(recv_src, "i32"), _addr(workspace, "i32"), int(spin_limit),
                                         ctypes.byref(bs), _stream(stream)), "llmoe_dispatch_signaled")
+
+
+def llmoe_dispatch_signaled_static(x, topk_idx, recv_x, recv_src, spin_limit: int, bs: llmoe_buf_set_t,
+                                   stream=None) -> None:
+    """llmoe_dispatch_signaled with the library's own fixed device workspace,
+    for callers that cannot allocate one (at most LLMOE_STATIC_MAX_RANKS
+    ranks; calls must not overlap on the GPU)."""
+    _check(_lib.llmoe_dispatch_signaled_static(_addr(x, "payload"), _addr(topk_idx, "i64"),
+                                               _addr(recv_x, "payload"), _addr(recv_src, "i32"), int(spin_limit),
+                                               ctypes.byref(bs), _stream(stream)), "llmoe_dispatch_signaled_static")
 
 
 def llmoe_clean(bs: llmoe_buf_set_t, stream=None) -> None:

@@ -264,6 +264,34 @@ LLMOE_API int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, vo
                                       void* workspace, int64_t spin_limit, const llmoe_buf_set_t* bs,
                                       llmoe_stream_t stream);
 
+/* Largest num_ranks llmoe_dispatch_signaled_static accepts. */
+#define LLMOE_STATIC_MAX_RANKS 1024
+
+/* llmoe_dispatch_signaled for callers that cannot allocate device memory.
+ * The pages have no counterpart for this call.
+ * Some callers have no way to obtain scratch memory at the point of the
+ * call: a plugin handed only raw device pointers by a host framework that
+ * owns every allocation, or a latency-critical loop in which a cudaMalloc,
+ * which may synchronize the device, is not acceptable.  This call needs no
+ * workspace from them: the per-source completion counters live in a fixed
+ * device array inside the library, sized for LLMOE_STATIC_MAX_RANKS ranks
+ * (4 KB, held by every GPU that loads the library until the process exits).
+ * It allocates nothing and calls no allocating routine.
+ *   - Same arguments and result as llmoe_dispatch_signaled, minus the
+ *     workspace.  num_ranks above LLMOE_STATIC_MAX_RANKS returns
+ *     LLMOE_ERR_INVALID_ARGUMENT without launching.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *     that first call before any stream capture.
+ *   - Each call clears the counters it uses (a cudaMemsetAsync on `stream`)
+ *     before its kernel, so a timed-out earlier call leaves no residue.
+ *   - All calls on a device share the one array: calls whose kernels
+ *     overlap on the GPU (on different streams) race on it and must not be
+ *     issued that way. */
+LLMOE_API int llmoe_dispatch_signaled_static(const void* x, const int64_t* topk_idx, void* recv_x,
+                                             int32_t* recv_src, int64_t spin_limit, const llmoe_buf_set_t* bs,
+                                             llmoe_stream_t stream);
+
 /* Clean (LLMoEBuffer::clean_meta): zero the num_experts int64 signal words
  * of buffer set `set` in each of the R rank buffers.  This resets both the
  * dispatch recv counts and the combine recv flags, which share the words. */
