@@ -620,6 +620,8 @@ __device__ __forceinline__ uint4 shfl_down16(const uint4& v) {
                     __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
 }
 
+constexpr int kUnpackBatch = 4;  // units whose loads a warp has in flight at once
+
 // Payload quad from two consecutive aligned quads a, b when the payload starts
 // `phase` words into a: words phase .. phase+3 of (a, b).
 __device__ __forceinline__ uint4 unshift_words(const uint4& a, const uint4& b, int phase) {
@@ -751,8 +753,6 @@ __global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, co
 // `msg0` (slot 0), into the rows starting at `row0`, headers into src0.  The
 // CTA's warps take (slot, chunk) units, four at a time so that each lane has
 // four loads in flight before it shuffles and stores.
-constexpr int kUnpackBatch = 4;
-
 __device__ __forceinline__ void unpack_bucket(const Geometry& g, const uint8_t* msg0, uint8_t* row0,
                                               int32_t* src0, int cnt, bool l2_only) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
@@ -788,7 +788,115 @@ __device__ __forceinline__ void unpack_bucket(const Geometry& g, const uint8_t* 
   }
 }
 
-// Unpack after a dispatch: CTA per bucket (expert e, source src), grid-stride;
+// Unpack after a dispatch, balanced over the grid: every CTA reads all E * R
+// bucket counts and their exclusive prefix (shared memory), so the N received
+// rows x chunks split evenly over all warps whatever the routing's skew; a
+// unit finds its bucket by binary search over the prefix.
+constexpr int kMaxScanBuckets = 8192;
+
+__device__ __forceinline__ int find_bucket(const int* pre, int nb, int r) {
+  int lo = 0, hi = nb - 1;  // largest b with pre[b] <= r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kThreads) unpack_balanced_kernel(Geometry g, void* __restrict__ recv_x,
+                                                                   int32_t* __restrict__ recv_src) {
+  __shared__ int s_pre[kMaxScanBuckets];
+  __shared__ int s_part[kThreads / 32];
+  release_next_grid();
+  wait_prior_grid();
+  const int nb = g.E * g.R;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int b = tid; b < nb; b += blockDim.x) {
+    const int e = b / g.R, src = b % g.R;
+    const int64_t c = reinterpret_cast<const int64_t*>(g.base + (e / g.L) * g.rank_stride + g.sig_off)
+        [(int64_t)(e % g.L) * g.R + src];
+    s_pre[b] = (int)max((int64_t)0, min(c, (int64_t)g.T_max));
+  }
+  __syncthreads();
+  // exclusive prefix: each thread scans a contiguous segment, the segment
+  // totals are scanned across the block
+  const int seg = (nb + blockDim.x - 1) / blockDim.x, lo = min(nb, tid * seg), hi = min(nb, lo + seg);
+  int sum = 0;
+  for (int b = lo; b < hi; ++b) sum += s_pre[b];
+  int incl = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) s_part[warp] = incl;
+  __syncthreads();
+  int warp_base = 0;
+  for (int w = 0; w < warp; ++w) warp_base += s_part[w];
+  int total = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += s_part[w];
+  int run = warp_base + incl - sum;
+  __syncthreads();  // every segment read its counts before any is overwritten
+  for (int b = lo; b < hi; ++b) {
+    const int c = s_pre[b];
+    s_pre[b] = run;
+    run += c;
+  }
+  __syncthreads();
+
+  // each warp takes a contiguous range of (row, chunk) units: one search for
+  // its first row's bucket, then a walk; four units' loads in flight at once
+  const int64_t nunits = (int64_t)total * g.nchunks;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + tid) >> 5;
+  const int64_t per = (nunits + nwarps - 1) / nwarps;
+  const int64_t ubeg = min(nunits, gw * per), uend = min(nunits, ubeg + per);
+  int bucket = ubeg < uend ? find_bucket(s_pre, nb, (int)(ubeg / g.nchunks)) : 0;
+  for (int64_t u0 = ubeg; u0 < uend; u0 += kUnpackBatch) {
+    uint4 a[kUnpackBatch], t4[kUnpackBatch];
+    const uint8_t* msgs[kUnpackBatch];
+    int64_t rows[kUnpackBatch];
+    int cs[kUnpackBatch];
+#pragma unroll
+    for (int i = 0; i < kUnpackBatch; ++i) {
+      const int64_t u = u0 + i;
+      a[i] = t4[i] = make_uint4(0, 0, 0, 0);
+      msgs[i] = nullptr;
+      if (u < uend) {
+        const int r = (int)(u / g.nchunks), c = (int)(u % g.nchunks);
+        while (bucket + 1 < nb && s_pre[bucket + 1] <= r) ++bucket;  // rows only grow along the range
+        const int slot = r - s_pre[bucket];
+        const int e = bucket / g.R, src = bucket % g.R, le = e % g.L;
+        const uint8_t* msg = g.base + (e / g.L) * g.rank_stride + g.recv_off +
+                             (((uint64_t)le * g.R + src) * g.T_max + slot) * g.msg;
+        msgs[i] = msg;
+        rows[i] = (int64_t)bucket * g.T_max + slot;
+        cs[i] = c;
+        const uintptr_t pa = reinterpret_cast<uintptr_t>(msg) + 4;
+        const int phase = (int)((pa >> 2) & 3);
+        const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
+        const int j = c * 32 + lane;
+        if (j < g.nq || (j == g.nq && phase != 0)) a[i] = __ldg(qb + j);
+        if (lane == 31 && phase != 0 && j < g.nq) t4[i] = __ldg(qb + j + 1);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kUnpackBatch; ++i) {
+      if (msgs[i] == nullptr) break;  // the whole warp
+      const int phase = (int)(((reinterpret_cast<uintptr_t>(msgs[i]) + 4) >> 2) & 3);
+      const int j = cs[i] * 32 + lane;
+      uint4 bq = shfl_down16(a[i]);
+      if (lane == 31) bq = t4[i];
+      if (j < g.nq)
+        reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(recv_x) + rows[i] * g.row_bytes)[j] =
+            unshift_words(a[i], bq, phase);
+      if (cs[i] == 0 && lane == 0) recv_src[rows[i]] = *reinterpret_cast<const int32_t*>(msgs[i]);
+    }
+  }
+}
+
+// Unpack after a dispatch with more buckets than the balanced kernel's
+// shared prefix holds: CTA per bucket (expert e, source src), grid-stride;
 // the bucket's count word gives how many of its slots hold a message.
 __global__ void __launch_bounds__(kThreads) unpack_kernel(Geometry g, void* __restrict__ recv_x,
                                                           int32_t* __restrict__ recv_src) {
@@ -1317,6 +1425,16 @@ int llmoe_unpack(void* recv_x, int32_t* recv_src, const llmoe_buf_set_t* bs, llm
   if (rc != LLMOE_SUCCESS) return rc;
   if (recv_x == nullptr || recv_src == nullptr || !aligned(recv_x, 16) || !aligned(recv_src, 4))
     return LLMOE_ERR_INVALID_ARGUMENT;
+  // the balanced kernel pays for a scan of every bucket count in every CTA;
+  // with at least as many buckets as routed entries there is little skew to
+  // balance and the per-bucket kernel is cheaper
+  const int64_t nb = (int64_t)g.E * g.R, entries = (int64_t)g.R * g.T * g.K;
+  if (nb <= kMaxScanBuckets && nb < entries) {
+    // one full wave: the copy is latency-bound, so every resident warp helps
+    const int64_t wave = (int64_t)num_sms() * blocks_per_sm(kslot(kUnpackKernel, 1),
+                                                            (const void*)unpack_balanced_kernel, kThreads, 0);
+    return launch(unpack_balanced_kernel, (unsigned)wave, kThreads, 0, stream, g, recv_x, recv_src);
+  }
   const int64_t wave =
       (int64_t)num_sms() * blocks_per_sm(kslot(kUnpackKernel), (const void*)unpack_kernel, kThreads, 0);
   const int64_t blocks = std::min<int64_t>(wave, (int64_t)g.E * g.R);
