@@ -1,29 +1,37 @@
 // llmoe.cu -- sm_103a kernels and the C ABI of libllmoe.so (see include/llmoe.h).
 //
 // One GPU holds R simulated expert-parallel ranks as R segments of one
-// allocation, each laid out as LLMoEBufferLayout<bf16> (LL_MoE_Buffers.hpp).
-// The data path is pure movement plus one fp32 multiply-add per byte pair, so
-// it is bound by HBM bandwidth: no tensor cores, 16-byte vector accesses,
-// every row read once.
+// allocation, each laid out as LLMoEBufferLayout<T> (LL_MoE_Buffers.hpp) for
+// a payload type T of bf16, fp16 or fp32.  The data path is data movement plus
+// one fp32 multiply-add per value in the combine, so it is bound by HBM
+// bandwidth and latency: 16-byte accesses, no tensor cores (nothing here is a
+// dense contraction).  Every launch uses programmatic dependent launch.
 //
 // Kernels:
-//   route scan (route_hist / route_slot, run at the start of the route,
-//     dispatch and combine kernels): per-(expert, source rank) counts and slots, where the
-//     slot of token t for expert e is the number of earlier tokens of the same
-//     source rank that chose e.  Built from a shared-memory histogram of the
-//     tokens before the CTA's block (integer atomics, so the result does not
-//     depend on their order) plus an in-block rank.  No global atomics, no
-//     scratch memory.
-//   dispatch_kernel: each warp moves 32 quads (512 B) of one token row per
-//     unit and writes them to the K destination messages.  A message is
-//     4 + 2H bytes, which is 4 (mod 16) for H % 8 == 0, so a destination row
-//     starts at any 4-byte phase; the warp shifts its quads by whole 32-bit
-//     words (neighbour quad via a shuffle) and issues aligned 16-byte stores,
-//     with 4/8-byte stores only at the head and tail of each message.
-//   combine_kernel: each warp reduces 32 quads of one output row: K aligned
-//     16-byte loads of expert rows, fp32 products rounded then added in
-//     ascending k (__fmul_rn / __fadd_rn: never contracted to an FMA), bf16
-//     round-to-nearest-even store.
+//   route scan (route_hist / route_slot, the prologue of the route, dispatch,
+//     combine, put and signalled kernels): per-(expert, source rank) counts
+//     and slots, where the slot of token t for expert e is the number of
+//     earlier tokens of the same source rank that chose e.  A shared-memory
+//     histogram of the tokens before the CTA's block (integer atomics: the
+//     result does not depend on their order) plus an in-block rank; no
+//     global atomics and no scratch memory.
+//   dispatch_kernel: one producer lane streams the CTA's x rows into a
+//     shared-memory ring (cp.async.bulk, mbarrier); each consumer thread owns a
+//     16-byte quad of a chunk and writes it to the token's K messages.  A
+//     message is 4 + H * sizeof(T) bytes, 4 (mod 16) when H * sizeof(T) is a
+//     multiple of 16, so a destination starts at any 4-byte phase: the quad is
+//     shifted by whole 32-bit words and stored aligned, with 4/8-byte stores
+//     only at a message's head and tail.
+//   combine_kernel<T>: each warp reduces 32 quads of one output row: up to 8
+//     aligned 16-byte loads of expert rows, fp32 products rounded then added
+//     in ascending k (__fmul_rn / __fadd_rn: never contracted to an FMA), the
+//     sum stored as T (bf16 / fp16 rounded to nearest even).
+//   combine_put_kernel, combine_reduce_kernel<T>: the staged combine through
+//     the combine receive buffers (messages realigned on write and on read).
+//   unpack_balanced_kernel, unpack_kernel: received messages to the experts'
+//     input layout, driven by the count words.
+//   dispatch_signaled_kernel: dispatch and unpack in one cooperative launch;
+//     CTAs signal each other through the count words, with bounded waits.
 //   clean_kernel: zeroes a set's R * E signal words (LLMoEBuffer::clean_meta).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -46,7 +54,7 @@ struct Geometry {
   uint64_t recv_off;     // this set's receive region, from a rank buffer's start
   uint64_t sig_off;      // this set's signal words
   uint64_t other_sig_off;  // the other set's signal words
-  uint64_t msg;          // 4 + 2H
+  uint64_t msg;          // 4 + H * sizeof(T)
   int32_t* err;          // optional error word
   uint32_t flags;        // LLMOE_FLAG_*
   int T_max, T, H, R, E, K, L;
@@ -72,7 +80,7 @@ __device__ __forceinline__ void report(int32_t* err, int32_t code) {
 __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void release_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Shared-memory view used by the three route-scan kernels.
+// Shared-memory view of the route scan.
 struct RouteSmem {
   int* hist;  // [E] tokens before the block (then: all tokens) per expert
   int* ent;   // [TB*K] the block's expert ids (-1 masked or invalid)
