@@ -628,7 +628,6 @@ __device__ __forceinline__ uint4 shfl_down16(const uint4& v) {
                     __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
 }
 
-constexpr int kUnpackBatch = 4;  // units whose loads a warp has in flight at once
 
 // Payload quad from two consecutive aligned quads a, b when the payload starts
 // `phase` words into a: words phase .. phase+3 of (a, b).
@@ -757,50 +756,20 @@ __global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, co
 // unpack, and the dispatch whose CTAs signal each other
 // ---------------------------------------------------------------------------
 
-// Unpacks one bucket (expert e, source src): its `cnt` messages, starting at
-// `msg0` (slot 0), into the rows starting at `row0`, headers into src0.  The
-// CTA's warps take (slot, chunk) units, four at a time so that each lane has
-// four loads in flight before it shuffles and stores.
-__device__ __forceinline__ void unpack_bucket(const Geometry& g, const uint8_t* msg0, uint8_t* row0,
-                                              int32_t* src0, int cnt, bool l2_only) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  const int n = cnt * g.nchunks;
-  for (int r0 = warp; r0 < n; r0 += kUnpackBatch * nwarps) {
-    uint4 a[kUnpackBatch], t[kUnpackBatch];
-#pragma unroll
-    for (int i = 0; i < kUnpackBatch; ++i) {
-      const int r = r0 + i * nwarps;
-      a[i] = t[i] = make_uint4(0, 0, 0, 0);
-      if (r < n) {
-        const int slot = r / g.nchunks, c = r % g.nchunks, j = c * 32 + lane;
-        const uintptr_t pa = reinterpret_cast<uintptr_t>(msg0 + (size_t)slot * g.msg) + 4;
-        const int phase = (int)((pa >> 2) & 3);
-        const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
-        if (j < g.nq || (j == g.nq && phase != 0)) a[i] = l2_only ? __ldcg(qb + j) : __ldg(qb + j);
-        if (lane == 31 && phase != 0 && j < g.nq) t[i] = l2_only ? __ldcg(qb + j + 1) : __ldg(qb + j + 1);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kUnpackBatch; ++i) {
-      const int r = r0 + i * nwarps;
-      if (r >= n) break;  // the whole warp
-      const int slot = r / g.nchunks, c = r % g.nchunks, j = c * 32 + lane;
-      const uint8_t* msg = msg0 + (size_t)slot * g.msg;
-      const int phase = (int)(((reinterpret_cast<uintptr_t>(msg) + 4) >> 2) & 3);
-      uint4 b = shfl_down16(a[i]);
-      if (lane == 31) b = t[i];
-      if (j < g.nq) reinterpret_cast<uint4*>(row0 + (size_t)slot * g.row_bytes)[j] = unshift_words(a[i], b, phase);
-      if (c == 0 && lane == 0)
-        src0[slot] = l2_only ? __ldcg(reinterpret_cast<const int32_t*>(msg)) : *reinterpret_cast<const int32_t*>(msg);
-    }
-  }
-}
-
 // Unpack after a dispatch, balanced over the grid: every CTA reads all E * R
 // bucket counts and their exclusive prefix (shared memory), so the N received
-// rows x chunks split evenly over all warps whatever the routing's skew; a
-// unit finds its bucket by binary search over the prefix.
+// rows x chunks split evenly over all warps whatever the routing's skew.  A
+// warp finds the bucket of its first row by binary search and then walks its
+// range row by row (unpack_row).
+#ifndef LLMOE_UNPACK_ROW_BATCH
+#define LLMOE_UNPACK_ROW_BATCH 8
+#endif
+#ifndef LLMOE_UNPACK_MIN_BLOCKS
+#define LLMOE_UNPACK_MIN_BLOCKS 4
+#endif
 constexpr int kMaxScanBuckets = 8192;
+constexpr int kUnpackRowBatch = LLMOE_UNPACK_ROW_BATCH;
+constexpr int kCountLoads = 8;  // count words a thread has in flight in the prologue
 
 __device__ __forceinline__ int find_bucket(const int* pre, int nb, int r) {
   int lo = 0, hi = nb - 1;  // largest b with pre[b] <= r
@@ -811,24 +780,85 @@ __device__ __forceinline__ int find_bucket(const int* pre, int nb, int r) {
   return lo;
 }
 
-__global__ void __launch_bounds__(kThreads) unpack_balanced_kernel(Geometry g, void* __restrict__ recv_x,
-                                                                   int32_t* __restrict__ recv_src) {
+__device__ __forceinline__ uint4 shfl_idx16(const uint4& v, int src_lane) {
+  return make_uint4(__shfl_sync(0xffffffffu, v.x, src_lane), __shfl_sync(0xffffffffu, v.y, src_lane),
+                    __shfl_sync(0xffffffffu, v.z, src_lane), __shfl_sync(0xffffffffu, v.w, src_lane));
+}
+
+// Moves chunks [c, cend) of one received message's payload to its row of the
+// experts' input: up to kUnpackRowBatch consecutive chunks per step, every
+// load of the step issued before the first store.  A lane's neighbour quad
+// comes from the next lane (shfl_down) and, for lane 31, from lane 0 of the
+// next chunk, so a step loads each aligned quad once.  kL2Only reads through
+// L2 only (the message may have been written by a CTA of the same launch).
+template <bool kL2Only>
+__device__ __forceinline__ void unpack_row(const Geometry& g, const uint8_t* msg, uint4* __restrict__ drow, int c,
+                                           int cend, int lane) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(msg) + 4;
+  const int phase = (int)((pa >> 2) & 3);
+  const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
+  auto ld = [](const uint4* q) { return kL2Only ? __ldcg(q) : __ldg(q); };
+  for (; c < cend; c += kUnpackRowBatch) {
+    const int n = min(kUnpackRowBatch, cend - c);
+    uint4 a[kUnpackRowBatch];
+#pragma unroll
+    for (int i = 0; i < kUnpackRowBatch; ++i) {
+      const int j = (c + i) * 32 + lane;
+      a[i] = make_uint4(0, 0, 0, 0);
+      if (i < n && (j < g.nq || (j == g.nq && phase != 0))) a[i] = ld(qb + j);
+    }
+    // lane 31 of the step's last chunk: the quad after it, unless past the payload
+    const int jl = (c + n - 1) * 32 + 31;
+    uint4 tail = make_uint4(0, 0, 0, 0);
+    if (lane == 31 && phase != 0 && jl < g.nq) tail = ld(qb + jl + 1);
+#pragma unroll
+    for (int i = 0; i < kUnpackRowBatch; ++i) {
+      if (i < n) {
+        const int j = (c + i) * 32 + lane;
+        uint4 q = a[i];
+        if (phase != 0) {
+          uint4 bq = shfl_down16(a[i]);
+          uint4 nx = tail;
+          if (i + 1 < kUnpackRowBatch) {
+            const uint4 t = shfl_idx16(a[min(i + 1, kUnpackRowBatch - 1)], 0);
+            if (i + 1 < n) nx = t;
+          }
+          if (lane == 31) bq = nx;
+          q = unshift_words(a[i], bq, phase);
+        }
+        if (j < g.nq) drow[j] = q;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, LLMOE_UNPACK_MIN_BLOCKS)
+    unpack_balanced_kernel(Geometry g, void* __restrict__ recv_x, int32_t* __restrict__ recv_src) {
   __shared__ int s_pre[kMaxScanBuckets];
   __shared__ int s_part[kThreads / 32];
   release_next_grid();
   wait_prior_grid();
   const int nb = g.E * g.R;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int b = tid; b < nb; b += blockDim.x) {
-    const int e = b / g.R, src = b % g.R;
-    const int64_t c = reinterpret_cast<const int64_t*>(g.base + (e / g.L) * g.rank_stride + g.sig_off)
-        [(int64_t)(e % g.L) * g.R + src];
-    s_pre[b] = (int)max((int64_t)0, min(c, (int64_t)g.T_max));
+  for (int b0 = 0; b0 < nb; b0 += kCountLoads * kThreads) {
+    int64_t c[kCountLoads];
+#pragma unroll
+    for (int i = 0; i < kCountLoads; ++i) {
+      const int b = b0 + i * kThreads + tid, e = b / g.R, src = b - e * g.R;
+      c[i] = b < nb ? reinterpret_cast<const int64_t*>(g.base + (e / g.L) * g.rank_stride + g.sig_off)
+                          [(int64_t)(e % g.L) * g.R + src]
+                    : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < kCountLoads; ++i) {
+      const int b = b0 + i * kThreads + tid;
+      if (b < nb) s_pre[b] = (int)max((int64_t)0, min(c[i], (int64_t)g.T_max));
+    }
   }
   __syncthreads();
   // exclusive prefix: each thread scans a contiguous segment, the segment
   // totals are scanned across the block
-  const int seg = (nb + blockDim.x - 1) / blockDim.x, lo = min(nb, tid * seg), hi = min(nb, lo + seg);
+  const int seg = (nb + kThreads - 1) / kThreads, lo = min(nb, tid * seg), hi = min(nb, lo + seg);
   int sum = 0;
   for (int b = lo; b < hi; ++b) sum += s_pre[b];
   int incl = sum;
@@ -842,83 +872,73 @@ __global__ void __launch_bounds__(kThreads) unpack_balanced_kernel(Geometry g, v
   int warp_base = 0;
   for (int w = 0; w < warp; ++w) warp_base += s_part[w];
   int total = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += s_part[w];
+  for (int w = 0; w < kThreads / 32; ++w) total += s_part[w];
   int run = warp_base + incl - sum;
   __syncthreads();  // every segment read its counts before any is overwritten
   for (int b = lo; b < hi; ++b) {
-    const int c = s_pre[b];
+    const int cb = s_pre[b];
     s_pre[b] = run;
-    run += c;
+    run += cb;
   }
   __syncthreads();
 
-  // each warp takes a contiguous range of (row, chunk) units: one search for
-  // its first row's bucket, then a walk; four units' loads in flight at once
+  // the warp's contiguous range [ubeg, uend) of (row, chunk) units
   const int64_t nunits = (int64_t)total * g.nchunks;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + tid) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  const int64_t gw = ((int64_t)blockIdx.x * kThreads + tid) >> 5;
   const int64_t per = (nunits + nwarps - 1) / nwarps;
   const int64_t ubeg = min(nunits, gw * per), uend = min(nunits, ubeg + per);
-  int bucket = ubeg < uend ? find_bucket(s_pre, nb, (int)(ubeg / g.nchunks)) : 0;
-  for (int64_t u0 = ubeg; u0 < uend; u0 += kUnpackBatch) {
-    uint4 a[kUnpackBatch], t4[kUnpackBatch];
-    const uint8_t* msgs[kUnpackBatch];
-    int64_t rows[kUnpackBatch];
-    int cs[kUnpackBatch];
-#pragma unroll
-    for (int i = 0; i < kUnpackBatch; ++i) {
-      const int64_t u = u0 + i;
-      a[i] = t4[i] = make_uint4(0, 0, 0, 0);
-      msgs[i] = nullptr;
-      if (u < uend) {
-        const int r = (int)(u / g.nchunks), c = (int)(u % g.nchunks);
-        while (bucket + 1 < nb && s_pre[bucket + 1] <= r) ++bucket;  // rows only grow along the range
-        const int slot = r - s_pre[bucket];
-        const int e = bucket / g.R, src = bucket % g.R, le = e % g.L;
-        const uint8_t* msg = g.base + (e / g.L) * g.rank_stride + g.recv_off +
-                             (((uint64_t)le * g.R + src) * g.T_max + slot) * g.msg;
-        msgs[i] = msg;
-        rows[i] = (int64_t)bucket * g.T_max + slot;
-        cs[i] = c;
-        const uintptr_t pa = reinterpret_cast<uintptr_t>(msg) + 4;
-        const int phase = (int)((pa >> 2) & 3);
-        const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
-        const int j = c * 32 + lane;
-        if (j < g.nq || (j == g.nq && phase != 0)) a[i] = __ldg(qb + j);
-        if (lane == 31 && phase != 0 && j < g.nq) t4[i] = __ldg(qb + j + 1);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kUnpackBatch; ++i) {
-      if (msgs[i] == nullptr) break;  // the whole warp
-      const int phase = (int)(((reinterpret_cast<uintptr_t>(msgs[i]) + 4) >> 2) & 3);
-      const int j = cs[i] * 32 + lane;
-      uint4 bq = shfl_down16(a[i]);
-      if (lane == 31) bq = t4[i];
-      if (j < g.nq)
-        reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(recv_x) + rows[i] * g.row_bytes)[j] =
-            unshift_words(a[i], bq, phase);
-      if (cs[i] == 0 && lane == 0) recv_src[rows[i]] = *reinterpret_cast<const int32_t*>(msgs[i]);
-    }
+  if (ubeg >= uend) return;
+  int r = (int)(ubeg / g.nchunks);
+  int c = (int)(ubeg - (int64_t)r * g.nchunks);
+  int64_t left = uend - ubeg;
+  int bucket = find_bucket(s_pre, nb, r);
+  while (left > 0) {
+    while (bucket + 1 < nb && s_pre[bucket + 1] <= r) ++bucket;  // rows only grow along the range
+    const int slot = r - s_pre[bucket];
+    const int e = bucket / g.R, src = bucket - e * g.R, le = e % g.L;
+    const uint8_t* msg = g.base + (e / g.L) * g.rank_stride + g.recv_off +
+                         (((uint64_t)le * g.R + src) * g.T_max + slot) * g.msg;
+    const int64_t orow = (int64_t)bucket * g.T_max + slot;
+    uint4* drow = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(recv_x) + orow * g.row_bytes);
+    const int cend = (int)min((int64_t)g.nchunks, c + left);  // this row's chunks in the range
+    const bool head = (c == 0);
+    int hv = 0;
+    if (head && lane == 0) hv = *reinterpret_cast<const int32_t*>(msg);
+    left -= cend - c;
+    unpack_row<false>(g, msg, drow, c, cend, lane);
+    if (head && lane == 0) recv_src[orow] = hv;
+    c = 0;
+    ++r;
   }
 }
 
-// Unpack after a dispatch with more buckets than the balanced kernel's
-// shared prefix holds: CTA per bucket (expert e, source src), grid-stride;
-// the bucket's count word gives how many of its slots hold a message.
-__global__ void __launch_bounds__(kThreads) unpack_kernel(Geometry g, void* __restrict__ recv_x,
+// Unpack after a dispatch with at least as many buckets as routed entries
+// (few rows per bucket, so little skew to balance), or more buckets than the
+// balanced kernel's shared prefix holds: one warp per bucket (expert e,
+// source src), grid-stride; the bucket's count word gives how many of its
+// slots hold a message, and the warp unpacks them row by row.
+__global__ void __launch_bounds__(kThreads, LLMOE_UNPACK_MIN_BLOCKS) unpack_kernel(Geometry g, void* __restrict__ recv_x,
                                                           int32_t* __restrict__ recv_src) {
   release_next_grid();
   wait_prior_grid();
-  const int64_t nbuckets = (int64_t)g.E * g.R;
-  for (int64_t bucket = blockIdx.x; bucket < nbuckets; bucket += gridDim.x) {
-    const int e = (int)(bucket / g.R), src = (int)(bucket % g.R), dst = e / g.L, le = e % g.L;
+  const int lane = threadIdx.x & 31;
+  const int nbuckets = g.E * g.R;  // E <= LLMOE_MAX_EXPERTS and R <= E: fits an int
+  const int nwarps = (gridDim.x * kThreads) >> 5;
+  for (int bucket = (blockIdx.x * kThreads + threadIdx.x) >> 5; bucket < nbuckets; bucket += nwarps) {
+    const int e = bucket / g.R, src = bucket - e * g.R, dst = e / g.L, le = e % g.L;
     const uint8_t* rank = g.base + dst * g.rank_stride;
     const int64_t c64 = reinterpret_cast<const int64_t*>(rank + g.sig_off)[(int64_t)le * g.R + src];
     const int cnt = (int)max((int64_t)0, min(c64, (int64_t)g.T_max));
     const uint8_t* msg0 = rank + g.recv_off + ((uint64_t)le * g.R + src) * g.T_max * g.msg;
-    uint8_t* row0 = reinterpret_cast<uint8_t*>(recv_x) + bucket * g.T_max * g.row_bytes;
-    unpack_bucket(g, msg0, row0, recv_src + bucket * g.T_max, cnt, false);
+    uint8_t* row0 = reinterpret_cast<uint8_t*>(recv_x) + (int64_t)bucket * g.T_max * g.row_bytes;
+    for (int slot = 0; slot < cnt; ++slot) {
+      const uint8_t* msg = msg0 + (size_t)slot * g.msg;
+      int hv = 0;
+      if (lane == 0) hv = *reinterpret_cast<const int32_t*>(msg);
+      unpack_row<false>(g, msg, reinterpret_cast<uint4*>(row0 + (size_t)slot * g.row_bytes), 0, g.nchunks, lane);
+      if (lane == 0) recv_src[(int64_t)bucket * g.T_max + slot] = hv;
+    }
   }
 }
 
@@ -938,16 +958,17 @@ __device__ __forceinline__ void st_release_gpu(long long* p, long long v) {
 // -(count + 1).  Consumer work takes buckets (expert e, source src) round
 // robin, waits (bounded) for the bucket's word, unpacks its rows and rewrites
 // the word to the plain count.
-__global__ void __launch_bounds__(kThreads) dispatch_signaled_kernel(Geometry g, const void* __restrict__ x,
+__global__ void __launch_bounds__(kThreads, 3) dispatch_signaled_kernel(Geometry g, const void* __restrict__ x,
                                                                      const int64_t* __restrict__ idx,
                                                                      void* __restrict__ recv_x,
                                                                      int32_t* __restrict__ recv_src,
-                                                                     int32_t* __restrict__ done, long long spin_limit) {
+                                                                     int32_t* __restrict__ done, long long spin_limit,
+                                                                     int warp_buckets) {
   extern __shared__ __align__(128) unsigned char smem[];
   const RouteSmem s = carve_route(smem, g);
   uintptr_t* s_dst = reinterpret_cast<uintptr_t*>(s.slot + g.TB * g.K + (g.E & 1));
   __shared__ int s_last;
-  __shared__ long long s_word;
+  __shared__ long long s_word[kThreads / 32];
 
   const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
@@ -1007,32 +1028,45 @@ __global__ void __launch_bounds__(kThreads) dispatch_signaled_kernel(Geometry g,
     if (threadIdx.x == 0) done[src] = 0;  // ready for the next call
   }
 
-  // ---- consumer: buckets (e, bsrc), round robin over the CTAs
+  // ---- consumer.  warp_buckets: one warp per bucket (e, bsrc), round robin
+  // over the grid's warps (few rows per bucket); else one CTA per bucket,
+  // round robin over the CTAs, the bucket's rows round robin over its warps
+  // (a hot bucket is spread)
   const int64_t nbuckets = (int64_t)g.E * g.R;
-  for (int64_t bucket = blockIdx.x; bucket < nbuckets; bucket += gridDim.x) {
+  const int64_t first = warp_buckets ? ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5 : blockIdx.x;
+  const int64_t step = warp_buckets ? ((int64_t)gridDim.x * kThreads) >> 5 : gridDim.x;
+  for (int64_t bucket = first; bucket < nbuckets; bucket += step) {
     const int e = (int)(bucket / g.R), bsrc = (int)(bucket % g.R), dst = e / g.L, le = e % g.L;
     uint8_t* rank = g.base + dst * g.rank_stride;
     long long* word = reinterpret_cast<long long*>(rank + g.sig_off) + ((int64_t)le * g.R + bsrc);
-    __syncthreads();  // s_word of the previous bucket has been read
-    if (threadIdx.x == 0) {
-      long long v = ld_acquire_gpu(word);
+    const bool waiter = warp_buckets ? lane == 0 : threadIdx.x == 0;
+    if (!warp_buckets) __syncthreads();  // s_word of the previous bucket has been read
+    long long v = 0;
+    if (waiter) {
+      v = ld_acquire_gpu(word);
       const long long start = clock64();
       while (v == 0 && clock64() - start <= spin_limit) {
         __nanosleep(64);
         v = ld_acquire_gpu(word);
       }
       if (v == 0) report(g.err, LLMOE_DEV_TIMEOUT);
-      s_word = v;
+      s_word[warp_buckets ? warp : 0] = v;
     }
-    __syncthreads();
-    const long long v = s_word;
+    // the bucket's readers come after the waiter's acquire
+    if (warp_buckets) __syncwarp(); else __syncthreads();
+    v = s_word[warp_buckets ? warp : 0];
     if (v >= 0) continue;  // timed out (0), or not a raised signal: leave the bucket
     const int cnt = (int)min(-v - 1, (long long)g.T_max);
-    unpack_bucket(g, rank + g.recv_off + ((uint64_t)le * g.R + bsrc) * g.T_max * g.msg,
-                  reinterpret_cast<uint8_t*>(recv_x) + bucket * g.T_max * g.row_bytes, recv_src + bucket * g.T_max,
-                  cnt, true);
-    __syncthreads();
-    if (threadIdx.x == 0) *word = -v - 1;  // the plain count, as a dispatch leaves it
+    const uint8_t* msg0 = rank + g.recv_off + ((uint64_t)le * g.R + bsrc) * g.T_max * g.msg;
+    uint8_t* row0 = reinterpret_cast<uint8_t*>(recv_x) + bucket * g.T_max * g.row_bytes;
+    for (int slot = warp_buckets ? 0 : warp; slot < cnt; slot += warp_buckets ? 1 : kThreads / 32) {
+      const uint8_t* msg = msg0 + (size_t)slot * g.msg;
+      int hv = 0;
+      if (lane == 0) hv = __ldcg(reinterpret_cast<const int32_t*>(msg));
+      unpack_row<true>(g, msg, reinterpret_cast<uint4*>(row0 + (size_t)slot * g.row_bytes), 0, g.nchunks, lane);
+      if (lane == 0) recv_src[bucket * g.T_max + slot] = hv;
+    }
+    if (waiter) *word = -v - 1;  // the plain count, as a dispatch leaves it
   }
 }
 
@@ -1445,7 +1479,7 @@ int llmoe_unpack(void* recv_x, int32_t* recv_src, const llmoe_buf_set_t* bs, llm
   }
   const int64_t wave =
       (int64_t)num_sms() * blocks_per_sm(kslot(kUnpackKernel), (const void*)unpack_kernel, kThreads, 0);
-  const int64_t blocks = std::min<int64_t>(wave, (int64_t)g.E * g.R);
+  const int64_t blocks = std::min<int64_t>(wave, ((int64_t)g.E * g.R + kThreads / 32 - 1) / (kThreads / 32));
   return launch(unpack_kernel, (unsigned)blocks, kThreads, 0, stream, g, recv_x, recv_src);
 }
 
@@ -1487,8 +1521,11 @@ int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, void* recv_x
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // consumers as llmoe_unpack: a warp per bucket when there are at least as
+  // many buckets as routed entries, else a CTA per bucket
+  const int warp_buckets = (int64_t)g.E * g.R >= (int64_t)g.R * g.T * g.K;
   if (cudaLaunchKernelEx(&cfg, dispatch_signaled_kernel, g, x, topk_idx, recv_x, recv_src,
-                         static_cast<int32_t*>(workspace), (long long)spin_limit) != cudaSuccess) {
+                         static_cast<int32_t*>(workspace), (long long)spin_limit, warp_buckets) != cudaSuccess) {
     cudaGetLastError();
     return LLMOE_ERR_CUDA;
   }
