@@ -17,10 +17,12 @@ gives the per-kernel times and the roofline.
 Printed (rank 0, one JSON line): the mean step time as ``value``; the
 effective HBM bandwidth of the algorithmic bytes; per-kernel times; the
 roofline of the dominant kernel against the measured copy bandwidth; the
-end-to-end time of the same round with host buffers (pinned host -> device
-copies of every input and device -> host read of the outputs inside the
-timed region); the CPU oracle timed on a bounded sample on the host; GPU
-clocks sampled during the timed region.
+end-to-end time of one MoE layer with identity experts through the C ABI
+with host buffers (x, topk_idx, topk_w copied from pinned host memory,
+dispatch, unpack, combine over the unpacked rows, output read back, all
+inside the timed region), and of the bench round with the dense expert
+outputs also uploaded; the CPU oracle timed on a bounded sample on the host;
+GPU clocks sampled during the timed region.
 
 --impl reference times the CPU oracle alone on the host cores (the
 reference arm; rank 0 only when launched with several ranks).
@@ -62,6 +64,7 @@ def parse_args(argv=None):
     p.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default="bf16", help="payload type T")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-e2e-dense-y", action="store_true", help="skip the e2e leg that uploads the dense y")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     return p.parse_args(argv)
@@ -564,50 +567,89 @@ def run_signaled(args, llmoe, w, x, idx, rb, es, flush, steps: int = 200):
 
 
 def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
-    """The same round with every input copied from pinned host memory and the
-    outputs (combine output, both sets' signal words) read back, per step."""
+    """Rounds through the C ABI with host buffers, per step: the inputs copied
+    from pinned host memory, the output (combine output, both sets' signal
+    words) read back.
+
+    e2e: one MoE layer with identity experts.  x, topk_idx and topk_w come from
+    the host; llmoe_dispatch (set 0), then llmoe_unpack lays the received rows
+    out as the experts' input, in the receive-row order the combine reads its
+    expert outputs in, and an identity expert's output is its input, so those
+    rows are the combine's y; llmoe_combine (set 1) returns
+    bf16(sum_k w_k x) per token.
+    e2e_dense_y: the bench round (dispatch + combine) with the dense expert
+    outputs y [E*R*T, H] also copied from the host every step."""
     import torch
 
     pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
     hx, hidx, hw = pin(inp["x"]), pin(inp["topk_idx"]), pin(inp["topk_w"])
-    hy = pin(dense_y(inp))
-    hout = torch.empty((w.R, tokens, w.H), dtype=torch.float32 if rb.msg_bytes - 4 == 4 * w.H else torch.int16
-                       ).pin_memory()
+    pay = torch.float32 if rb.msg_bytes - 4 == 4 * w.H else torch.int16
+    hout = torch.empty((w.R, tokens, w.H), dtype=pay).pin_memory()
     hsig = torch.empty((2, w.R, w.E), dtype=torch.int64).pin_memory()
     dx, didx, dw = torch.empty_like(hx, device="cuda"), torch.empty_like(hidx, device="cuda"), torch.empty_like(
         hw, device="cuda")
-    dy = torch.empty_like(hy, device="cuda")
     dout = torch.empty_like(hout, device="cuda")
+    rows = w.E * w.R * w.T
+    recv_x = torch.empty((rows, w.H), dtype=pay, device="cuda")
+    recv_src = torch.empty((rows,), dtype=torch.int32, device="cuda")
     F = llmoe.LLMOE_FLAG_CLEAN_OTHER_SET
     bs0 = rb.buf_set(0, w.K, flags=F)
     bs1 = rb.buf_set(1, w.K, flags=F | llmoe.LLMOE_FLAG_INPUTS_READY)
-    h2d = sum(t.numel() * t.element_size() for t in (hx, hidx, hw, hy))
     d2h = hout.numel() * hout.element_size() + hsig.numel() * hsig.element_size()
 
-    def step():
-        for d, h in ((dx, hx), (didx, hidx), (dw, hw), (dy, hy)):
-            d.copy_(h, non_blocking=True)
-        llmoe.llmoe_dispatch(dx, didx, bs0, stream)
-        llmoe.llmoe_combine(dy, didx, dw, dout, bs1, stream)
+    def read_back():
         hout.copy_(dout, non_blocking=True)
         hsig[0].copy_(rb.signal_words(0), non_blocking=True)
         hsig[1].copy_(rb.signal_words(1), non_blocking=True)
 
-    llmoe.llmoe_clean(rb.buf_set(0, w.K), stream)
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    n = max(3, args.e2e_steps)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    for a, b in evs:
-        a.record(stream)
-        step()
-        b.record(stream)
-    torch.cuda.synchronize()
-    us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
-    return {"value": round(us, 2), "unit": "us/round", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n, "note": "inputs x, topk_idx, topk_w and the dense expert outputs y copied host->device "
-                                "every step; output and signal words copied back"}
+    def layer():
+        for d, h in ((dx, hx), (didx, hidx), (dw, hw)):
+            d.copy_(h, non_blocking=True)
+        llmoe.llmoe_dispatch(dx, didx, bs0, stream)
+        llmoe.llmoe_unpack(recv_x, recv_src, bs0, stream)
+        llmoe.llmoe_combine(recv_x, didx, dw, dout, bs1, stream)
+        read_back()
+
+    def timed(step):
+        llmoe.llmoe_clean(rb.buf_set(0, w.K), stream)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        n = max(3, args.e2e_steps)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3, n
+
+    us, n = timed(layer)
+    res = {"value": round(us, 2), "unit": "us/round",
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hx, hidx, hw)),
+           "d2h_bytes_per_step": d2h, "steps": n, "launches_per_step": 3,
+           "note": "one MoE layer with identity experts through the C ABI: x, topk_idx, topk_w copied "
+                   "host->device; llmoe_dispatch; llmoe_unpack (the experts' input rows, which identity experts "
+                   "return as their output y); llmoe_combine over them; output and signal words copied back"}
+    del recv_x, recv_src
+    if not args.no_e2e_dense_y:
+        hy = pin(dense_y(inp))
+        dy = torch.empty_like(hy, device="cuda")
+
+        def round_dense_y():
+            for d, h in ((dx, hx), (didx, hidx), (dw, hw), (dy, hy)):
+                d.copy_(h, non_blocking=True)
+            llmoe.llmoe_dispatch(dx, didx, bs0, stream)
+            llmoe.llmoe_combine(dy, didx, dw, dout, bs1, stream)
+            read_back()
+
+        us2, n2 = timed(round_dense_y)
+        res["dense_y"] = {"value": round(us2, 2), "unit": "us/round",
+                          "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hx, hidx, hw, hy)),
+                          "d2h_bytes_per_step": d2h, "steps": n2,
+                          "note": "the bench round with the dense expert outputs y [E*R*T, H] also copied "
+                                  "host->device every step"}
+    return res
 
 
 def main(argv=None):

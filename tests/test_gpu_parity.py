@@ -609,7 +609,7 @@ def check_unpack(r: Round, recv_x, recv_src):
 
 
 @pytest.mark.parametrize("name,dtype", [("tiny", "bf16"), ("dsv3", "bf16"), ("skewed", "bf16"), ("many_small", "bf16"),
-                                        ("skewed", "fp32"), ("many_small", "fp16")])
+                                        ("skewed", "fp32"), ("many_small", "fp16"), ("large", "bf16")])
 def test_unpack_after_dispatch(L, name, dtype):
     w = WORKLOADS[name]
     r = Round(L, w, seed=81, dtype=dtype)
@@ -639,6 +639,64 @@ def test_dispatch_signaled(L, name, dtype):
         d = r.check_dispatch()  # messages and plain counts, as llmoe_dispatch leaves them
         check_unpack(r, recv_x, recv_src)
     r.check_canary(d)
+
+
+# odd shapes for both unpack kernels (balanced when buckets are fewer than
+# routed entries, else per bucket) and the signalled dispatch: payloads of
+# 1, 7, 33, 125 and 385 quads (partial chunks, a row shorter than one step,
+# rows ending mid-step), every message phase, masks, one to 32 ranks
+UNPACK_SHAPES = [s for s in SWEEP if s[4] == 37] + [(2, 8, 3, 1000, 41, "bf16"), (3, 15, 4, 3080, 19, "bf16"),
+                                                    (2, 8, 2, 252, 23, "fp32"), (4, 8, 3, 264, 9, "fp16")]
+UNPACK_SHAPES = [s if len(s) == 6 else (*s, "bf16") for s in UNPACK_SHAPES]
+
+
+@pytest.mark.parametrize("R,E,K,H,T,dtype", UNPACK_SHAPES)
+def test_unpack_shapes(L, R, E, K, H, T, dtype):
+    w = Workload("unpack_shape", R, T, H, E, K, mask_p=0.3 if K > 1 else 0.0)
+    r = Round(L, w, seed=R * 100 + E + K + H + T, dtype=dtype)
+    recv_x, recv_src = unpack_buffers(w, dtype)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch(r.x, r.idx, r.bs_d)
+    L.llmoe_unpack(recv_x, recv_src, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    r.check_dispatch()
+    check_unpack(r, recv_x, recv_src)
+    recv_x2, recv_src2 = unpack_buffers(w, dtype)
+    ws = torch.zeros(L.llmoe_signal_workspace_bytes(r.bs_d) // 4, dtype=torch.int32, device="cuda")
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch_signaled(r.x, r.idx, recv_x2, recv_src2, ws, 2_000_000_000, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    r.check_dispatch()
+    check_unpack(r, recv_x2, recv_src2)
+
+
+@pytest.mark.parametrize("name,dtype", [("tiny", "bf16"), ("dsv3", "bf16"), ("skewed", "bf16"), ("many_small", "fp16")])
+def test_identity_expert_layer(L, name, dtype):
+    # dispatch -> unpack -> combine over the unpacked rows: an identity expert
+    # returns its input, so the unpacked rows are the combine's y (the
+    # end-to-end layer the benchmark times); both fused cleans on
+    w = WORKLOADS[name]
+    r = Round(L, w, seed=85, dtype=dtype)
+    recv_x, recv_src = unpack_buffers(w, dtype)
+    F = L.LLMOE_FLAG_CLEAN_OTHER_SET
+    bs0 = r.rb.buf_set(0, w.K, r.T_call, r.err, flags=F)
+    bs1 = r.rb.buf_set(1, w.K, r.T_call, r.err, flags=F | L.LLMOE_FLAG_INPUTS_READY)
+    L.llmoe_clean(r.bs_d)
+    for rep in range(2):
+        L.llmoe_dispatch(r.x, r.idx, bs0)
+        L.llmoe_unpack(recv_x, recv_src, bs0)
+        L.llmoe_combine(recv_x, r.idx, r.wt, r.out, bs1)
+        torch.cuda.synchronize()
+        assert r.error() == 0
+        u = oracle.unpack(r.inp["x"], r.inp["topk_idx"], w.E, num_max_tokens=w.T, dtype=dtype)
+        ref, flags = oracle.combine(u["recv_x"], r.inp["topk_idx"], r.inp["topk_w"], w.H, w.E, num_max_tokens=w.T,
+                                    dtype=dtype)
+        dist = ulp_distance(r.out.cpu().numpy(), ref, dtype)
+        assert dist.max(initial=0) == 0, f"{int((dist != 0).sum())} elements differ"
+        assert np.array_equal(r.rb.signal_words(1).cpu().numpy(), flags)
+        assert not r.rb.signal_words(0).any(), "the combine zeroed the dispatch set's counts"
 
 
 def test_dispatch_signaled_times_out_without_signals(L):
