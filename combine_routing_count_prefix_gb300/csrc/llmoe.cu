@@ -475,20 +475,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void axpy_quad(float (&acc)[8], float w, const uint4& v) {
-  acc[0] = __fadd_rn(acc[0], __fmul_rn(w, bf16lo(v.x)));
-  acc[1] = __fadd_rn(acc[1], __fmul_rn(w, bf16hi(v.x)));
-  acc[2] = __fadd_rn(acc[2], __fmul_rn(w, bf16lo(v.y)));
-  acc[3] = __fadd_rn(acc[3], __fmul_rn(w, bf16hi(v.y)));
-  acc[4] = __fadd_rn(acc[4], __fmul_rn(w, bf16lo(v.z)));
-  acc[5] = __fadd_rn(acc[5], __fmul_rn(w, bf16hi(v.z)));
-  acc[6] = __fadd_rn(acc[6], __fmul_rn(w, bf16lo(v.w)));
-  acc[7] = __fadd_rn(acc[7], __fmul_rn(w, bf16hi(v.w)));
+#ifndef LLMOE_PACKED_F32X2
+#define LLMOE_PACKED_F32X2 1
+#endif
+#if LLMOE_PACKED_F32X2
+// Both products in one instruction (mul.rn.f32x2: each lane rounded as
+// __fmul_rn rounds it), then the two sums as separate __fadd_rn.  A packed
+// add after the packed multiply is fused into one packed FMA by the
+// assembler, which changes the rounding, so the sums stay scalar.
+__device__ __forceinline__ void axpy2(float& a0, float& a1, float w, float y0, float y1) {
+  float p0, p1;
+  asm("{\n\t.reg .b64 y, w2;\n\tmov.b64 y, {%2, %3};\n\tmov.b64 w2, {%4, %4};\n\t"
+      "mul.rn.f32x2 y, y, w2;\n\tmov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(p0), "=f"(p1)
+      : "f"(y0), "f"(y1), "f"(w));
+  a0 = __fadd_rn(a0, p0);
+  a1 = __fadd_rn(a1, p1);
 }
+#else
+__device__ __forceinline__ void axpy2(float& a0, float& a1, float w, float y0, float y1) {
+  a0 = __fadd_rn(a0, __fmul_rn(w, y0));
+  a1 = __fadd_rn(a1, __fmul_rn(w, y1));
+}
+#endif
 
-// One warp reduces 32 quads (512 B) of one output row per unit: up to
-// kKBatch expert rows are loaded (16 B per lane each) before they are
-// accumulated, in ascending k.
 // One 16-byte quad of payload values, by payload type: accumulate w * value
 // into acc in fp32 (product rounded, then sum rounded: never fused), and pack
 // the accumulators back (bf16 / fp16 round to nearest even; fp32 kept).
@@ -496,7 +506,10 @@ template <int DT>
 __device__ __forceinline__ void axpy_q(float (&acc)[8], float w, const uint4& v);
 template <>
 __device__ __forceinline__ void axpy_q<LLMOE_DTYPE_BF16>(float (&acc)[8], float w, const uint4& v) {
-  axpy_quad(acc, w, v);
+  axpy2(acc[0], acc[1], w, bf16lo(v.x), bf16hi(v.x));
+  axpy2(acc[2], acc[3], w, bf16lo(v.y), bf16hi(v.y));
+  axpy2(acc[4], acc[5], w, bf16lo(v.z), bf16hi(v.z));
+  axpy2(acc[6], acc[7], w, bf16lo(v.w), bf16hi(v.w));
 }
 template <>
 __device__ __forceinline__ void axpy_q<LLMOE_DTYPE_FP16>(float (&acc)[8], float w, const uint4& v) {
@@ -504,16 +517,13 @@ __device__ __forceinline__ void axpy_q<LLMOE_DTYPE_FP16>(float (&acc)[8], float 
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[i]));  // exact
-    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, f.x));
-    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, f.y));
+    axpy2(acc[2 * i], acc[2 * i + 1], w, f.x, f.y);
   }
 }
 template <>
 __device__ __forceinline__ void axpy_q<LLMOE_DTYPE_FP32>(float (&acc)[8], float w, const uint4& v) {
-  acc[0] = __fadd_rn(acc[0], __fmul_rn(w, __uint_as_float(v.x)));
-  acc[1] = __fadd_rn(acc[1], __fmul_rn(w, __uint_as_float(v.y)));
-  acc[2] = __fadd_rn(acc[2], __fmul_rn(w, __uint_as_float(v.z)));
-  acc[3] = __fadd_rn(acc[3], __fmul_rn(w, __uint_as_float(v.w)));
+  axpy2(acc[0], acc[1], w, __uint_as_float(v.x), __uint_as_float(v.y));
+  axpy2(acc[2], acc[3], w, __uint_as_float(v.z), __uint_as_float(v.w));
 }
 
 template <int DT>
@@ -540,6 +550,9 @@ constexpr int kCmbThreads = LLMOE_CMB_THREADS;
 constexpr int kCmbWarps = kCmbThreads / 32;
 constexpr int kKBatch = 8;
 
+// One warp reduces 32 quads (512 B) of one output row per unit: up to
+// kKBatch expert rows are loaded (16 B per lane each) before they are
+// accumulated, in ascending k.
 template <int DT>
 __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const void* __restrict__ y,
                                                               const int64_t* __restrict__ idx,
@@ -627,6 +640,19 @@ __device__ __forceinline__ uint4 shfl_down16(const uint4& v) {
   return make_uint4(__shfl_down_sync(0xffffffffu, v.x, 1), __shfl_down_sync(0xffffffffu, v.y, 1),
                     __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
 }
+__device__ __forceinline__ uint4 shfl_idx16(const uint4& v, int src_lane) {
+  return make_uint4(__shfl_sync(0xffffffffu, v.x, src_lane), __shfl_sync(0xffffffffu, v.y, src_lane),
+                    __shfl_sync(0xffffffffu, v.z, src_lane), __shfl_sync(0xffffffffu, v.w, src_lane));
+}
+
+// Rows move in steps of up to kRowBatch 512-byte chunks per warp (put, unpack).
+#ifndef LLMOE_ROW_BATCH
+#define LLMOE_ROW_BATCH 8
+#endif
+#ifndef LLMOE_UNPACK_MIN_BLOCKS
+#define LLMOE_UNPACK_MIN_BLOCKS 4
+#endif
+constexpr int kRowBatch = LLMOE_ROW_BATCH;
 
 
 // Payload quad from two consecutive aligned quads a, b when the payload starts
@@ -644,8 +670,8 @@ __device__ __forceinline__ uint4 unshift_words(const uint4& a, const uint4& b, i
 // combine_recv[e][t] (row e * T_max + t of its receive region).  One warp
 // moves 32 quads of one entry's row per unit; rank src's flag words are
 // written by the CTA of its last token block.
-__global__ void __launch_bounds__(kThreads) combine_put_kernel(Geometry g, const void* __restrict__ y,
-                                                               const int64_t* __restrict__ idx) {
+__global__ void __launch_bounds__(kThreads, 4) combine_put_kernel(Geometry g, const void* __restrict__ y,
+                                                                  const int64_t* __restrict__ idx) {
   extern __shared__ __align__(128) unsigned char smem[];
   const RouteSmem s = carve_route(smem, g);
   const int TBK = g.TB * g.K;
@@ -679,17 +705,35 @@ __global__ void __launch_bounds__(kThreads) combine_put_kernel(Geometry g, const
   clean_other_set(g);
   if (last) route_count_block(s, nblock);
 
+  // one warp per entry: its expert row in steps of up to kRowBatch
+  // chunks, every load of a step before its first store; lane 0's previous
+  // quad is lane 31's quad of the chunk before (the header word t before
+  // chunk 0)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nunits = nblock * g.nchunks;
-  for (int u = warp; u < nunits; u += kThreads / 32) {
-    const int q = u / g.nchunks, c = u % g.nchunks;
+  for (int q = warp; q < nblock; q += kThreads / 32) {
     const uint4* row = s_src[q];
     if (row == nullptr) continue;  // the whole warp: masked entry
-    const int t = t0 + q / g.K, j = c * 32 + lane;
-    const uint4 cur = j < g.nq ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
-    uint4 prev = shfl_up16(cur);
-    if (lane == 0) prev = j == 0 ? make_uint4(0, 0, 0, (uint32_t)t) : __ldg(row + j - 1);
-    if (j < g.nq) put_quad(s_dst[q], j, g.nq, prev, cur);
+    const uintptr_t d = s_dst[q];
+    uint4 carry = make_uint4(0, 0, 0, (uint32_t)(t0 + q / g.K));
+    for (int c = 0; c < g.nchunks; c += kRowBatch) {
+      const int n = min(kRowBatch, g.nchunks - c);
+      uint4 cur[kRowBatch];
+#pragma unroll
+      for (int i = 0; i < kRowBatch; ++i) {
+        const int j = (c + i) * 32 + lane;
+        cur[i] = (i < n && j < g.nq) ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < kRowBatch; ++i) {
+        if (i < n) {
+          const int j = (c + i) * 32 + lane;
+          uint4 prev = shfl_up16(cur[i]);
+          if (lane == 0) prev = carry;
+          if (j < g.nq) put_quad(d, j, g.nq, prev, cur[i]);
+          carry = shfl_idx16(cur[i], 31);
+        }
+      }
+    }
   }
 
   if (last) {
@@ -704,19 +748,24 @@ __global__ void __launch_bounds__(kThreads) combine_put_kernel(Geometry g, const
 // One warp per (token, 32-quad chunk); the messages sit at 4-byte phases, so
 // each lane loads its aligned quad, takes the next one from its neighbour and
 // shifts the payload words into place.
+#ifndef LLMOE_REDUCE_KBATCH
+#define LLMOE_REDUCE_KBATCH 4
+#endif
+constexpr int kReduceBatch = LLMOE_REDUCE_KBATCH;  // messages whose loads a warp has in flight at once
+
 template <int DT>
-__global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, const int64_t* __restrict__ idx,
-                                                                  const float* __restrict__ topk_w,
-                                                                  void* __restrict__ out) {
+__global__ void __launch_bounds__(kThreads, 4) combine_reduce_kernel(Geometry g, const int64_t* __restrict__ idx,
+                                                                     const float* __restrict__ topk_w,
+                                                                     void* __restrict__ out) {
   release_next_grid();
   wait_prior_grid();
   const int lane = threadIdx.x & 31;
   const int64_t nunits = (int64_t)g.R * g.T * g.nchunks;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < nunits; u += nwarps) {
-    const int c = (int)(u % g.nchunks);
     const int64_t tok = u / g.nchunks;
-    const int src = (int)(tok / g.T), t = (int)(tok % g.T);
+    const int c = (int)(u - tok * g.nchunks);
+    const int src = (int)(tok / g.T), t = (int)(tok - (int64_t)src * g.T);
     long long e_lane = -1;
     float w_lane = 0.0f;
     if (lane < g.K) {
@@ -728,23 +777,38 @@ __global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, co
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    for (int k = 0; k < g.K; ++k) {  // ascending k
-      const long long e = __shfl_sync(0xffffffffu, e_lane, k);
-      const float wk = __shfl_sync(0xffffffffu, w_lane, k);
-      if (e < 0 || e >= g.E) continue;  // the whole warp
-      const uint8_t* msg = rbase + ((uint64_t)e * g.T_max + t) * g.msg;
-      const uintptr_t pa = reinterpret_cast<uintptr_t>(msg) + 4;
-      const int phase = (int)((pa >> 2) & 3);
-      const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
-      // lane j holds aligned quad j; the quad past the payload end feeds the
-      // last lane when the payload is not aligned
-      uint4 a = make_uint4(0, 0, 0, 0);
-      if (j < g.nq || (j == g.nq && phase != 0)) a = __ldg(qb + j);
-      uint4 b = shfl_down16(a);
-      if (lane == 31 && phase != 0 && j < g.nq) b = __ldg(qb + j + 1);
-      if (g.err != nullptr && j == 0 && *reinterpret_cast<const int32_t*>(msg) != t)
-        report(g.err, LLMOE_DEV_BAD_MESSAGE);
-      if (j < g.nq) axpy_q<DT>(acc, wk, unshift_words(a, b, phase));
+    for (int k0 = 0; k0 < g.K; k0 += kReduceBatch) {
+      // the batch's messages: lane j holds aligned quad j; the quad past the
+      // payload end feeds the last lane when the payload is not aligned
+      uint4 a[kReduceBatch], tl[kReduceBatch];
+      const uint8_t* msg[kReduceBatch];
+      float wk[kReduceBatch];
+#pragma unroll
+      for (int i = 0; i < kReduceBatch; ++i) {
+        const int k = k0 + i;
+        const long long e = __shfl_sync(0xffffffffu, e_lane, k & 31);
+        wk[i] = __shfl_sync(0xffffffffu, w_lane, k & 31);
+        a[i] = tl[i] = make_uint4(0, 0, 0, 0);
+        msg[i] = nullptr;
+        if (k < g.K && e >= 0 && e < g.E) {  // the whole warp
+          msg[i] = rbase + ((uint64_t)e * g.T_max + t) * g.msg;
+          const uintptr_t pa = reinterpret_cast<uintptr_t>(msg[i]) + 4;
+          const int phase = (int)((pa >> 2) & 3);
+          const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
+          if (j < g.nq || (j == g.nq && phase != 0)) a[i] = __ldg(qb + j);
+          if (lane == 31 && phase != 0 && j < g.nq) tl[i] = __ldg(qb + j + 1);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kReduceBatch; ++i) {  // ascending k
+        if (msg[i] == nullptr) continue;
+        const int phase = (int)(((reinterpret_cast<uintptr_t>(msg[i]) + 4) >> 2) & 3);
+        uint4 b = shfl_down16(a[i]);
+        if (lane == 31) b = tl[i];
+        if (g.err != nullptr && j == 0 && *reinterpret_cast<const int32_t*>(msg[i]) != t)
+          report(g.err, LLMOE_DEV_BAD_MESSAGE);
+        if (j < g.nq) axpy_q<DT>(acc, wk[i], unshift_words(a[i], b, phase));
+      }
     }
     if (j < g.nq)
       reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + ((int64_t)src * g.T + t) * g.row_bytes)[j] =
@@ -761,14 +825,7 @@ __global__ void __launch_bounds__(kThreads) combine_reduce_kernel(Geometry g, co
 // rows x chunks split evenly over all warps whatever the routing's skew.  A
 // warp finds the bucket of its first row by binary search and then walks its
 // range row by row (unpack_row).
-#ifndef LLMOE_UNPACK_ROW_BATCH
-#define LLMOE_UNPACK_ROW_BATCH 8
-#endif
-#ifndef LLMOE_UNPACK_MIN_BLOCKS
-#define LLMOE_UNPACK_MIN_BLOCKS 4
-#endif
 constexpr int kMaxScanBuckets = 8192;
-constexpr int kUnpackRowBatch = LLMOE_UNPACK_ROW_BATCH;
 constexpr int kCountLoads = 8;  // count words a thread has in flight in the prologue
 
 __device__ __forceinline__ int find_bucket(const int* pre, int nb, int r) {
@@ -780,13 +837,9 @@ __device__ __forceinline__ int find_bucket(const int* pre, int nb, int r) {
   return lo;
 }
 
-__device__ __forceinline__ uint4 shfl_idx16(const uint4& v, int src_lane) {
-  return make_uint4(__shfl_sync(0xffffffffu, v.x, src_lane), __shfl_sync(0xffffffffu, v.y, src_lane),
-                    __shfl_sync(0xffffffffu, v.z, src_lane), __shfl_sync(0xffffffffu, v.w, src_lane));
-}
 
 // Moves chunks [c, cend) of one received message's payload to its row of the
-// experts' input: up to kUnpackRowBatch consecutive chunks per step, every
+// experts' input: up to kRowBatch consecutive chunks per step, every
 // load of the step issued before the first store.  A lane's neighbour quad
 // comes from the next lane (shfl_down) and, for lane 31, from lane 0 of the
 // next chunk, so a step loads each aligned quad once.  kL2Only reads through
@@ -798,11 +851,11 @@ __device__ __forceinline__ void unpack_row(const Geometry& g, const uint8_t* msg
   const int phase = (int)((pa >> 2) & 3);
   const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
   auto ld = [](const uint4* q) { return kL2Only ? __ldcg(q) : __ldg(q); };
-  for (; c < cend; c += kUnpackRowBatch) {
-    const int n = min(kUnpackRowBatch, cend - c);
-    uint4 a[kUnpackRowBatch];
+  for (; c < cend; c += kRowBatch) {
+    const int n = min(kRowBatch, cend - c);
+    uint4 a[kRowBatch];
 #pragma unroll
-    for (int i = 0; i < kUnpackRowBatch; ++i) {
+    for (int i = 0; i < kRowBatch; ++i) {
       const int j = (c + i) * 32 + lane;
       a[i] = make_uint4(0, 0, 0, 0);
       if (i < n && (j < g.nq || (j == g.nq && phase != 0))) a[i] = ld(qb + j);
@@ -812,15 +865,15 @@ __device__ __forceinline__ void unpack_row(const Geometry& g, const uint8_t* msg
     uint4 tail = make_uint4(0, 0, 0, 0);
     if (lane == 31 && phase != 0 && jl < g.nq) tail = ld(qb + jl + 1);
 #pragma unroll
-    for (int i = 0; i < kUnpackRowBatch; ++i) {
+    for (int i = 0; i < kRowBatch; ++i) {
       if (i < n) {
         const int j = (c + i) * 32 + lane;
         uint4 q = a[i];
         if (phase != 0) {
           uint4 bq = shfl_down16(a[i]);
           uint4 nx = tail;
-          if (i + 1 < kUnpackRowBatch) {
-            const uint4 t = shfl_idx16(a[min(i + 1, kUnpackRowBatch - 1)], 0);
+          if (i + 1 < kRowBatch) {
+            const uint4 t = shfl_idx16(a[min(i + 1, kRowBatch - 1)], 0);
             if (i + 1 < n) nx = t;
           }
           if (lane == 31) bq = nx;
@@ -918,8 +971,8 @@ __global__ void __launch_bounds__(kThreads, LLMOE_UNPACK_MIN_BLOCKS)
 // balanced kernel's shared prefix holds: one warp per bucket (expert e,
 // source src), grid-stride; the bucket's count word gives how many of its
 // slots hold a message, and the warp unpacks them row by row.
-__global__ void __launch_bounds__(kThreads, LLMOE_UNPACK_MIN_BLOCKS) unpack_kernel(Geometry g, void* __restrict__ recv_x,
-                                                          int32_t* __restrict__ recv_src) {
+__global__ void __launch_bounds__(kThreads, LLMOE_UNPACK_MIN_BLOCKS)
+    unpack_kernel(Geometry g, void* __restrict__ recv_x, int32_t* __restrict__ recv_src) {
   release_next_grid();
   wait_prior_grid();
   const int lane = threadIdx.x & 31;
@@ -959,11 +1012,11 @@ __device__ __forceinline__ void st_release_gpu(long long* p, long long v) {
 // robin, waits (bounded) for the bucket's word, unpacks its rows and rewrites
 // the word to the plain count.
 __global__ void __launch_bounds__(kThreads, 3) dispatch_signaled_kernel(Geometry g, const void* __restrict__ x,
-                                                                     const int64_t* __restrict__ idx,
-                                                                     void* __restrict__ recv_x,
-                                                                     int32_t* __restrict__ recv_src,
-                                                                     int32_t* __restrict__ done, long long spin_limit,
-                                                                     int warp_buckets) {
+                                                                        const int64_t* __restrict__ idx,
+                                                                        void* __restrict__ recv_x,
+                                                                        int32_t* __restrict__ recv_src,
+                                                                        int32_t* __restrict__ done, long long spin_limit,
+                                                                        int warp_buckets) {
   extern __shared__ __align__(128) unsigned char smem[];
   const RouteSmem s = carve_route(smem, g);
   uintptr_t* s_dst = reinterpret_cast<uintptr_t*>(s.slot + g.TB * g.K + (g.E & 1));
