@@ -357,6 +357,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         clean1()
         combine_plain()
 
+    # the same round captured once as a CUDA graph (two kernel nodes with a
+    # programmatic edge), replayed per step
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        llmoe.llmoe_dispatch(x, idx, bs0)
+        llmoe.llmoe_combine(y, idx, wt, out, bs1)
+
     clean0()  # once, before the first round
     for _ in range(args.warmup):
         flush()
@@ -372,7 +379,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         return [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
 
     ev, ev4, evk = new_events(args.steps, 2), new_events(args.steps, 2), new_events(args.steps, 3)
-    evs = new_events(args.steps, 2)
+    evs, evg = new_events(args.steps, 2), new_events(args.steps, 2)
     with ClockSampler(gpu_id_for(local_rank)) as clocks:
         torch.cuda.synchronize()
         if world > 1:
@@ -404,6 +411,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             e[1].record(stream)
             combine()
             e[2].record(stream)
+        # the round replayed from its CUDA graph
+        for e in evg:
+            flush()
+            e[0].record(stream)
+            graph.replay()
+            e[1].record(stream)
         # the staged combine (messages through combine_recv[e][t], then the reduction)
         for e in evs:
             flush()
@@ -413,6 +426,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             e[1].record(stream)
         torch.cuda.synchronize()
     staged_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    graph_ms = [e[0].elapsed_time(e[1]) for e in evg]
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     four_ms = [e[0].elapsed_time(e[1]) for e in ev4]
     disp_ms = [e[0].elapsed_time(e[1]) for e in evk]
@@ -448,7 +462,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                        "round": "llmoe_dispatch(set 0) + llmoe_combine(set 1), each zeroing the other set's "
                                 "signal words (LLMOE_FLAG_CLEAN_OTHER_SET: the llmoe_clean calls fused); combine "
                                 "with LLMOE_FLAG_INPUTS_READY; round_us_four_calls: clean, dispatch, clean, "
-                                "combine as four calls",
+                                "combine as four calls; round_us_cuda_graph: the two-launch round captured "
+                                "once as a CUDA graph and replayed",
                        "timing": "value: CUDA events around each round; per-kernel times and roofline: a second "
                                  "pass with events around every kernel, same step count"},
             "effective_gbs": round(gbs, 1), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
@@ -456,6 +471,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "algorithmic_bytes_per_round": algo["round"],
             "dispatch_us": round(d_us, 3), "combine_us": round(c_us, 3),
             "round_us_four_calls": round(statistics.mean(four_ms) * 1e3, 3),
+            "round_us_cuda_graph": round(statistics.mean(graph_ms) * 1e3, 3),
             "staged_combine_us": round(statistics.mean(staged_ms) * 1e3, 3),
             "staged_combine_gbs": round((algo["combine"] + 2 * n_valid * (4 + es * w.H)) /
                                         (statistics.mean(staged_ms) * 1e3) / 1e3, 1),
