@@ -500,7 +500,9 @@ def run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es, micro_batches: i
     clean, combine on one set each) against the two-stream double-buffered
     schedule, where micro-batch b+1's dispatch overlaps micro-batch b's
     combine (sets b % 2).  No L2 flush between micro-batches: this is the
-    steady state of a pipeline."""
+    steady state of a pipeline.  Each schedule is timed as issued from Python
+    (eager) and replayed from a CUDA graph captured once (both streams join
+    the capture), which takes the host's issue rate out of the figure."""
     import torch
 
     from combine_routing_count_prefix_gb300.pipeline import DoubleBufferPipeline
@@ -508,9 +510,9 @@ def run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es, micro_batches: i
     outs = [torch.empty((w.R, tokens, w.H), dtype=torch.float32 if es == 4 else torch.int16, device="cuda")
             for _ in (0, 1)]
     bs = [rb.buf_set(s, w.K) for s in (0, 1)]
-    cur = torch.cuda.current_stream()
 
     def serial():
+        cur = torch.cuda.current_stream()
         for b in range(micro_batches):
             s = b % 2
             llmoe.llmoe_clean(bs[s], cur)
@@ -518,27 +520,42 @@ def run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es, micro_batches: i
             llmoe.llmoe_clean(bs[s], cur)
             llmoe.llmoe_combine(y, idx, wt, outs[s], bs[s], cur)
 
-    pipe = DoubleBufferPipeline(rb, w.K)
+    # one schedule for eager calls, a fresh one for the capture: a captured
+    # stream may only wait on events recorded inside the same capture
+    pipes = {False: DoubleBufferPipeline(rb, w.K), True: DoubleBufferPipeline(rb, w.K)}
 
     def pipelined():
+        pipe = pipes[torch.cuda.is_current_stream_capturing()]
         for b in range(micro_batches):
             pipe.dispatch(b, x, idx)
             pipe.combine(b, y, idx, wt, outs[b % 2])
         pipe.join()
 
+    def timed(run):
+        cur = torch.cuda.current_stream()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        run()
+        b_.record(cur)
+        torch.cuda.synchronize()
+        return round(a.elapsed_time(b_) * 1e3 / micro_batches, 3)
+
     res = {}
     for name, fn in (("serial", serial), ("pipelined", pipelined)):
         fn()  # warm-up
         torch.cuda.synchronize()
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(cur)
-        fn()
-        b_.record(cur)
+        res[f"{name}_us_per_microbatch_eager"] = timed(fn)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        graph.replay()
         torch.cuda.synchronize()
-        res[f"{name}_us_per_microbatch"] = round(a.elapsed_time(b_) * 1e3 / micro_batches, 3)
+        res[f"{name}_us_per_microbatch"] = timed(graph.replay)
+        del graph
     res["micro_batches"] = micro_batches
     res["note"] = ("micro-batch b uses buffer set b % 2; pipelined: dispatches on one stream, combines on another, "
-                   "b+1's dispatch overlapping b's combine; no L2 flush between micro-batches")
+                   "b+1's dispatch overlapping b's combine; no L2 flush between micro-batches; *_us_per_microbatch: "
+                   "the schedule replayed from a CUDA graph; *_eager: issued from Python call by call")
     return res
 
 

@@ -748,6 +748,21 @@ __global__ void __launch_bounds__(kThreads, 4) combine_put_kernel(Geometry g, co
 // One warp per (token, 32-quad chunk); the messages sit at 4-byte phases, so
 // each lane loads its aligned quad, takes the next one from its neighbour and
 // shifts the payload words into place.
+// Payload quad j of a message whose payload starts `phase` 32-bit words past
+// a 16-byte boundary, read with the widest loads that alignment allows (one
+// 16-byte, two 8-byte or four 4-byte loads).  The phase is the same for the
+// whole warp, so the branch does not diverge.
+__device__ __forceinline__ uint4 ld_payload_quad(const uint8_t* pay, int phase, int j) {
+  const uint8_t* p = pay + 16 * (size_t)j;
+  if (phase == 0) return __ldg(reinterpret_cast<const uint4*>(p));
+  if (phase == 2) {
+    const uint2 lo = __ldg(reinterpret_cast<const uint2*>(p)), hi = __ldg(reinterpret_cast<const uint2*>(p + 8));
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
+  }
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+  return make_uint4(__ldg(w), __ldg(w + 1), __ldg(w + 2), __ldg(w + 3));
+}
+
 #ifndef LLMOE_REDUCE_KBATCH
 #define LLMOE_REDUCE_KBATCH 4
 #endif
@@ -778,9 +793,9 @@ __global__ void __launch_bounds__(kThreads, 4) combine_reduce_kernel(Geometry g,
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
     for (int k0 = 0; k0 < g.K; k0 += kReduceBatch) {
-      // the batch's messages: lane j holds aligned quad j; the quad past the
-      // payload end feeds the last lane when the payload is not aligned
-      uint4 a[kReduceBatch], tl[kReduceBatch];
+      // the batch's messages: lane j reads payload quad j at the message's
+      // own alignment
+      uint4 a[kReduceBatch];
       const uint8_t* msg[kReduceBatch];
       float wk[kReduceBatch];
 #pragma unroll
@@ -788,26 +803,20 @@ __global__ void __launch_bounds__(kThreads, 4) combine_reduce_kernel(Geometry g,
         const int k = k0 + i;
         const long long e = __shfl_sync(0xffffffffu, e_lane, k & 31);
         wk[i] = __shfl_sync(0xffffffffu, w_lane, k & 31);
-        a[i] = tl[i] = make_uint4(0, 0, 0, 0);
+        a[i] = make_uint4(0, 0, 0, 0);
         msg[i] = nullptr;
         if (k < g.K && e >= 0 && e < g.E) {  // the whole warp
           msg[i] = rbase + ((uint64_t)e * g.T_max + t) * g.msg;
-          const uintptr_t pa = reinterpret_cast<uintptr_t>(msg[i]) + 4;
-          const int phase = (int)((pa >> 2) & 3);
-          const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
-          if (j < g.nq || (j == g.nq && phase != 0)) a[i] = __ldg(qb + j);
-          if (lane == 31 && phase != 0 && j < g.nq) tl[i] = __ldg(qb + j + 1);
+          const int phase = (int)(((reinterpret_cast<uintptr_t>(msg[i]) + 4) >> 2) & 3);
+          if (j < g.nq) a[i] = ld_payload_quad(msg[i] + 4, phase, j);
         }
       }
 #pragma unroll
       for (int i = 0; i < kReduceBatch; ++i) {  // ascending k
         if (msg[i] == nullptr) continue;
-        const int phase = (int)(((reinterpret_cast<uintptr_t>(msg[i]) + 4) >> 2) & 3);
-        uint4 b = shfl_down16(a[i]);
-        if (lane == 31) b = tl[i];
         if (g.err != nullptr && j == 0 && *reinterpret_cast<const int32_t*>(msg[i]) != t)
           report(g.err, LLMOE_DEV_BAD_MESSAGE);
-        if (j < g.nq) axpy_q<DT>(acc, wk[i], unshift_words(a[i], b, phase));
+        if (j < g.nq) axpy_q<DT>(acc, wk[i], a[i]);
       }
     }
     if (j < g.nq)

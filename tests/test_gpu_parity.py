@@ -537,8 +537,11 @@ def test_payload_types_shapes(L, dtype, H, R, E, K, T):
 # overlapping b's combine
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name,H", [("tiny", 256), ("skewed", 512), ("many_small", 256)])
-def test_double_buffer_pipeline(L, name, H):
+@pytest.mark.parametrize("name,H,graph", [("tiny", 256, False), ("skewed", 512, False), ("many_small", 256, False),
+                                          ("skewed", 512, True)])
+def test_double_buffer_pipeline(L, name, H, graph):
+    # graph: the whole two-stream schedule captured once as a CUDA graph (both
+    # streams join the capture) and replayed twice
     from combine_routing_count_prefix_gb300.pipeline import DoubleBufferPipeline
 
     w = WORKLOADS[name].with_(H=H)
@@ -550,19 +553,30 @@ def test_double_buffer_pipeline(L, name, H):
     dev_in = [(dev(b["x"]), dev(b["topk_idx"]), dev(b["topk_w"]), y_dev(b)) for b in batches]
     outs = [torch.full((w.R, w.T, w.H), OUT_CANARY, dtype=torch.int16, device="cuda") for _ in range(M)]
     snaps, flags = [None] * M, [None] * M
-    for b in range(M):
-        x, idx, wt, y = dev_in[b]
-        s = b % 2
 
-        def snap_dispatch(b=b, s=s):
-            snaps[b] = (rb.recv_rows(s).clone(), rb.signal_words(s).clone())
+    def schedule():
+        for b in range(M):
+            x, idx, wt, y = dev_in[b]
+            s = b % 2
 
-        def snap_flags(b=b, s=s):
-            flags[b] = rb.signal_words(s).clone()
+            def snap_dispatch(b=b, s=s):
+                snaps[b] = (rb.recv_rows(s).clone(), rb.signal_words(s).clone())
 
-        pipe.dispatch(b, x, idx, after=snap_dispatch)
-        pipe.combine(b, y, idx, wt, outs[b], after=snap_flags)
-    pipe.join()
+            def snap_flags(b=b, s=s):
+                flags[b] = rb.signal_words(s).clone()
+
+            pipe.dispatch(b, x, idx, after=snap_dispatch)
+            pipe.combine(b, y, idx, wt, outs[b], after=snap_flags)
+        pipe.join()
+
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            schedule()
+        for _ in range(2):
+            g.replay()
+    else:
+        schedule()
     torch.cuda.synchronize()
     assert L.llmoe_get_error(pipe.bs[0]) == 0
     for b in range(M):
