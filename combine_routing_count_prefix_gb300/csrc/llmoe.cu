@@ -848,47 +848,70 @@ __device__ __forceinline__ int find_bucket(const int* pre, int nb, int r) {
 
 
 // Moves chunks [c, cend) of one received message's payload to its row of the
-// experts' input: up to kRowBatch consecutive chunks per step, every
-// load of the step issued before the first store.  A lane's neighbour quad
-// comes from the next lane (shfl_down) and, for lane 31, from lane 0 of the
-// next chunk, so a step loads each aligned quad once.  kL2Only reads through
-// L2 only (the message may have been written by a CTA of the same launch).
+// experts' input: up to kRowBatch consecutive chunks per step, every load of
+// the step issued before the first store.
+// - Through L1 (kL2Only false): lane j reads payload quad j at the message's
+//   own alignment (ld_payload_quad); the narrower loads of one quad hit the
+//   lines its first load brought into L1.
+// - L2 only (kL2Only true: the message may have been written by a CTA of the
+//   same launch, so no L1 copy may be used): every aligned quad is loaded
+//   once, and lane j rebuilds its quad from its own aligned quad and the next,
+//   which comes from the next lane (shfl_down) or, for lane 31, from lane 0 of
+//   the next chunk.  Narrow loads there would fetch each quad's sectors from
+//   L2 up to four times.
 template <bool kL2Only>
 __device__ __forceinline__ void unpack_row(const Geometry& g, const uint8_t* msg, uint4* __restrict__ drow, int c,
                                            int cend, int lane) {
-  const uintptr_t pa = reinterpret_cast<uintptr_t>(msg) + 4;
-  const int phase = (int)((pa >> 2) & 3);
-  const uint4* qb = reinterpret_cast<const uint4*>(pa & ~(uintptr_t)15);
-  auto ld = [](const uint4* q) { return kL2Only ? __ldcg(q) : __ldg(q); };
-  for (; c < cend; c += kRowBatch) {
-    const int n = min(kRowBatch, cend - c);
-    uint4 a[kRowBatch];
+  const uint8_t* pay = msg + 4;
+  const int phase = (int)((reinterpret_cast<uintptr_t>(pay) >> 2) & 3);
+  if constexpr (!kL2Only) {
+    for (; c < cend; c += kRowBatch) {
+      const int n = min(kRowBatch, cend - c);
+      uint4 a[kRowBatch];
 #pragma unroll
-    for (int i = 0; i < kRowBatch; ++i) {
-      const int j = (c + i) * 32 + lane;
-      a[i] = make_uint4(0, 0, 0, 0);
-      if (i < n && (j < g.nq || (j == g.nq && phase != 0))) a[i] = ld(qb + j);
-    }
-    // lane 31 of the step's last chunk: the quad after it, unless past the payload
-    const int jl = (c + n - 1) * 32 + 31;
-    uint4 tail = make_uint4(0, 0, 0, 0);
-    if (lane == 31 && phase != 0 && jl < g.nq) tail = ld(qb + jl + 1);
-#pragma unroll
-    for (int i = 0; i < kRowBatch; ++i) {
-      if (i < n) {
+      for (int i = 0; i < kRowBatch; ++i) {
         const int j = (c + i) * 32 + lane;
-        uint4 q = a[i];
-        if (phase != 0) {
-          uint4 bq = shfl_down16(a[i]);
-          uint4 nx = tail;
-          if (i + 1 < kRowBatch) {
-            const uint4 t = shfl_idx16(a[min(i + 1, kRowBatch - 1)], 0);
-            if (i + 1 < n) nx = t;
+        a[i] = make_uint4(0, 0, 0, 0);
+        if (i < n && j < g.nq) a[i] = ld_payload_quad(pay, phase, j);
+      }
+#pragma unroll
+      for (int i = 0; i < kRowBatch; ++i) {
+        const int j = (c + i) * 32 + lane;
+        if (i < n && j < g.nq) drow[j] = a[i];
+      }
+    }
+  } else {
+    const uint4* qb = reinterpret_cast<const uint4*>(reinterpret_cast<uintptr_t>(pay) & ~(uintptr_t)15);
+    for (; c < cend; c += kRowBatch) {
+      const int n = min(kRowBatch, cend - c);
+      uint4 a[kRowBatch];
+#pragma unroll
+      for (int i = 0; i < kRowBatch; ++i) {
+        const int j = (c + i) * 32 + lane;
+        a[i] = make_uint4(0, 0, 0, 0);
+        if (i < n && (j < g.nq || (j == g.nq && phase != 0))) a[i] = __ldcg(qb + j);
+      }
+      // lane 31 of the step's last chunk: the quad after it, unless past the payload
+      const int jl = (c + n - 1) * 32 + 31;
+      uint4 tail = make_uint4(0, 0, 0, 0);
+      if (lane == 31 && phase != 0 && jl < g.nq) tail = __ldcg(qb + jl + 1);
+#pragma unroll
+      for (int i = 0; i < kRowBatch; ++i) {
+        if (i < n) {
+          const int j = (c + i) * 32 + lane;
+          uint4 q = a[i];
+          if (phase != 0) {
+            uint4 bq = shfl_down16(a[i]);
+            uint4 nx = tail;
+            if (i + 1 < kRowBatch) {
+              const uint4 t = shfl_idx16(a[min(i + 1, kRowBatch - 1)], 0);
+              if (i + 1 < n) nx = t;
+            }
+            if (lane == 31) bq = nx;
+            q = unshift_words(a[i], bq, phase);
           }
-          if (lane == 31) bq = nx;
-          q = unshift_words(a[i], bq, phase);
+          if (j < g.nq) drow[j] = q;
         }
-        if (j < g.nq) drow[j] = q;
       }
     }
   }
