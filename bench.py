@@ -601,26 +601,31 @@ def run_signaled(args, llmoe, w, x, idx, rb, es, flush, steps: int = 200):
 
 def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
     """Rounds through the C ABI with host buffers, per step: the inputs copied
-    from pinned host memory, the output (combine output, both sets' signal
-    words) read back.
+    from pinned host memory, the result (the combine output) read back.
 
-    e2e: one MoE layer with identity experts.  x, topk_idx and topk_w come from
-    the host; llmoe_dispatch (set 0), then llmoe_unpack lays the received rows
-    out as the experts' input, in the receive-row order the combine reads its
-    expert outputs in, and an identity expert's output is its input, so those
-    rows are the combine's y; llmoe_combine (set 1) returns
-    bf16(sum_k w_k x) per token.
+    e2e: one MoE layer with identity experts.  x, topk_idx and topk_w sit in
+    one pinned host buffer and go up in one copy; llmoe_dispatch (set 0), then
+    llmoe_unpack lays the received rows out as the experts' input, in the
+    receive-row order the combine reads its expert outputs in, and an identity
+    expert's output is its input, so those rows are the combine's y;
+    llmoe_combine (set 1) returns bf16(sum_k w_k x) per token, and the output
+    comes back in one copy.
     e2e_dense_y: the bench round (dispatch + combine) with the dense expert
     outputs y [E*R*T, H] also copied from the host every step."""
     import torch
 
-    pin = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
-    hx, hidx, hw = pin(inp["x"]), pin(inp["topk_idx"]), pin(inp["topk_w"])
+    x, idx, wts = inp["x"], inp["topk_idx"], inp["topk_w"]
+    x_b, idx_b, w_b = x.nbytes, idx.nbytes, wts.nbytes  # x: whole 16-byte rows; idx: 8-byte words
+    hin = torch.empty(x_b + idx_b + w_b, dtype=torch.uint8).pin_memory()
+    hin[:x_b].copy_(torch.from_numpy(np.ascontiguousarray(x).view(np.uint8).reshape(-1)))
+    hin[x_b:x_b + idx_b].copy_(torch.from_numpy(np.ascontiguousarray(idx).view(np.uint8).reshape(-1)))
+    hin[x_b + idx_b:].copy_(torch.from_numpy(np.ascontiguousarray(wts).view(np.uint8).reshape(-1)))
+    din = torch.empty_like(hin, device="cuda")
     pay = torch.float32 if rb.msg_bytes - 4 == 4 * w.H else torch.int16
+    dx = din[:x_b].view(pay).view(w.R, tokens, w.H)
+    didx = din[x_b:x_b + idx_b].view(torch.int64).view(w.R, tokens, w.K)
+    dw = din[x_b + idx_b:].view(torch.float32).view(w.R, tokens, w.K)
     hout = torch.empty((w.R, tokens, w.H), dtype=pay).pin_memory()
-    hsig = torch.empty((2, w.R, w.E), dtype=torch.int64).pin_memory()
-    dx, didx, dw = torch.empty_like(hx, device="cuda"), torch.empty_like(hidx, device="cuda"), torch.empty_like(
-        hw, device="cuda")
     dout = torch.empty_like(hout, device="cuda")
     rows = w.E * w.R * w.T
     recv_x = torch.empty((rows, w.H), dtype=pay, device="cuda")
@@ -628,20 +633,14 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
     F = llmoe.LLMOE_FLAG_CLEAN_OTHER_SET
     bs0 = rb.buf_set(0, w.K, flags=F)
     bs1 = rb.buf_set(1, w.K, flags=F | llmoe.LLMOE_FLAG_INPUTS_READY)
-    d2h = hout.numel() * hout.element_size() + hsig.numel() * hsig.element_size()
-
-    def read_back():
-        hout.copy_(dout, non_blocking=True)
-        hsig[0].copy_(rb.signal_words(0), non_blocking=True)
-        hsig[1].copy_(rb.signal_words(1), non_blocking=True)
+    d2h = hout.numel() * hout.element_size()
 
     def layer():
-        for d, h in ((dx, hx), (didx, hidx), (dw, hw)):
-            d.copy_(h, non_blocking=True)
+        din.copy_(hin, non_blocking=True)
         llmoe.llmoe_dispatch(dx, didx, bs0, stream)
         llmoe.llmoe_unpack(recv_x, recv_src, bs0, stream)
         llmoe.llmoe_combine(recv_x, didx, dw, dout, bs1, stream)
-        read_back()
+        hout.copy_(dout, non_blocking=True)
 
     def timed(step):
         llmoe.llmoe_clean(rb.buf_set(0, w.K), stream)
@@ -658,27 +657,27 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
         return statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3, n
 
     us, n = timed(layer)
-    res = {"value": round(us, 2), "unit": "us/round",
-           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hx, hidx, hw)),
+    res = {"value": round(us, 2), "unit": "us/round", "h2d_bytes_per_step": hin.numel(),
            "d2h_bytes_per_step": d2h, "steps": n, "launches_per_step": 3,
            "note": "one MoE layer with identity experts through the C ABI: x, topk_idx, topk_w copied "
-                   "host->device; llmoe_dispatch; llmoe_unpack (the experts' input rows, which identity experts "
-                   "return as their output y); llmoe_combine over them; output and signal words copied back"}
+                   "host->device in one copy from one pinned buffer; llmoe_dispatch; llmoe_unpack (the experts' "
+                   "input rows, which identity experts return as their output y); llmoe_combine over them; the "
+                   "output copied back"}
     del recv_x, recv_src
     if not args.no_e2e_dense_y:
-        hy = pin(dense_y(inp))
+        hy = torch.from_numpy(dense_y(inp).view(np.int16) if pay == torch.int16 else dense_y(inp)).pin_memory()
         dy = torch.empty_like(hy, device="cuda")
 
         def round_dense_y():
-            for d, h in ((dx, hx), (didx, hidx), (dw, hw), (dy, hy)):
-                d.copy_(h, non_blocking=True)
+            din.copy_(hin, non_blocking=True)
+            dy.copy_(hy, non_blocking=True)
             llmoe.llmoe_dispatch(dx, didx, bs0, stream)
             llmoe.llmoe_combine(dy, didx, dw, dout, bs1, stream)
-            read_back()
+            hout.copy_(dout, non_blocking=True)
 
         us2, n2 = timed(round_dense_y)
         res["dense_y"] = {"value": round(us2, 2), "unit": "us/round",
-                          "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hx, hidx, hw, hy)),
+                          "h2d_bytes_per_step": hin.numel() + hy.numel() * hy.element_size(),
                           "d2h_bytes_per_step": d2h, "steps": n2,
                           "note": "the bench round with the dense expert outputs y [E*R*T, H] also copied "
                                   "host->device every step"}
