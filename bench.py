@@ -379,7 +379,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         return [[torch.cuda.Event(enable_timing=True) for _ in range(k)] for _ in range(n)]
 
     ev, ev4, evk = new_events(args.steps, 2), new_events(args.steps, 2), new_events(args.steps, 3)
-    evs, evg = new_events(args.steps, 2), new_events(args.steps, 2)
+    evs, evg, evf = new_events(args.steps, 2), new_events(args.steps, 2), new_events(args.steps, 2)
     with ClockSampler(gpu_id_for(local_rank)) as clocks:
         torch.cuda.synchronize()
         if world > 1:
@@ -411,6 +411,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             e[1].record(stream)
             combine()
             e[2].record(stream)
+        # the combine alone after its own flush (the dispatch's dirty lines
+        # written back first, outside the events)
+        for e in evf:
+            flush()
+            dispatch()
+            flush()
+            e[0].record(stream)
+            combine()
+            e[1].record(stream)
         # the round replayed from its CUDA graph
         for e in evg:
             flush()
@@ -427,6 +436,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         torch.cuda.synchronize()
     staged_ms = [e[0].elapsed_time(e[1]) for e in evs]
     graph_ms = [e[0].elapsed_time(e[1]) for e in evg]
+    comb_flushed_ms = [e[0].elapsed_time(e[1]) for e in evf]
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     four_ms = [e[0].elapsed_time(e[1]) for e in ev4]
     disp_ms = [e[0].elapsed_time(e[1]) for e in evk]
@@ -465,11 +475,13 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                 "combine as four calls; round_us_cuda_graph: the two-launch round captured "
                                 "once as a CUDA graph and replayed",
                        "timing": "value: CUDA events around each round; per-kernel times and roofline: a second "
-                                 "pass with events around every kernel, same step count"},
+                                 "pass with events around every kernel, same step count; combine_us_l2_flushed: "
+                                 "the combine with L2 flushed between it and the dispatch"},
             "effective_gbs": round(gbs, 1), "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
             "frac_of_measured_hbm": round(gbs / peak, 4),
             "algorithmic_bytes_per_round": algo["round"],
             "dispatch_us": round(d_us, 3), "combine_us": round(c_us, 3),
+            "combine_us_l2_flushed": round(statistics.mean(comb_flushed_ms) * 1e3, 3),
             "round_us_four_calls": round(statistics.mean(four_ms) * 1e3, 3),
             "round_us_cuda_graph": round(statistics.mean(graph_ms) * 1e3, 3),
             "staged_combine_us": round(statistics.mean(staged_ms) * 1e3, 3),
@@ -483,6 +495,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
             "gpu_launches": 2 * args.steps,
             "clocks": clocks.summary(),
         }
+        cf_us = statistics.mean(comb_flushed_ms) * 1e3
+        line["kernels"] = {  # every kernel of the round against the same measured peak
+            "dispatch_kernel": {"us": round(d_us, 3), "gbs": round(algo["dispatch"] / d_us / 1e3, 1),
+                                "frac": round(algo["dispatch"] / d_us / 1e3 / peak, 4)},
+            "combine_kernel": {"us": round(c_us, 3), "gbs": round(algo["combine"] / c_us / 1e3, 1),
+                               "frac": round(algo["combine"] / c_us / 1e3 / peak, 4)},
+            "combine_kernel_l2_flushed": {"us": round(cf_us, 3), "gbs": round(algo["combine"] / cf_us / 1e3, 1),
+                                          "frac": round(algo["combine"] / cf_us / 1e3 / peak, 4)}}
         line["double_buffer"] = pipe
         line["dispatch_unpack"] = signaled
         if e2e is not None:
