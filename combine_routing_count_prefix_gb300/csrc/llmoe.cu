@@ -39,6 +39,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 
 #include "llmoe.h"
@@ -1227,15 +1228,22 @@ int dtype_size(int dtype) {
   }
 }
 
-int g_num_sms[64] = {0};
+// Per-device caches of device queries.  Host threads may call the library
+// concurrently: every entry is an atomic, and two threads that miss together
+// both query and store the same value.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_num_sms[kMaxDevices];
 
 int num_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
-  if (dev < 64 && g_num_sms[dev] > 0) return g_num_sms[dev];
+  if (dev < kMaxDevices) {
+    const int c = g_num_sms[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  if (dev < 64) g_num_sms[dev] = n;
+  if (dev < kMaxDevices) g_num_sms[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -1303,20 +1311,26 @@ void set_blocking(Geometry* g, int blocks_per_sm) {
   g->nblk = g->T > 0 ? (g->T + g->TB - 1) / g->TB : 1;
 }
 
-int g_smem_optin[64][32] = {{0}};
+constexpr int kMaxSlots = 32;  // kslot values: kernel id * 4 + payload type
+std::atomic<int> g_smem_optin[kMaxDevices][kMaxSlots];
 
 // Opts a kernel in to more than 48 KB of dynamic shared memory (once per
-// device and size).
+// device and size; the largest size opted in so far is kept).
 int set_smem(int id, const void* fn, size_t bytes) {
   if (bytes <= 48 * 1024) return LLMOE_SUCCESS;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LLMOE_ERR_CUDA;
-  if (dev >= 0 && dev < 64 && (size_t)g_smem_optin[dev][id] >= bytes) return LLMOE_SUCCESS;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && (size_t)g_smem_optin[dev][id].load(std::memory_order_relaxed) >= bytes) return LLMOE_SUCCESS;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
     cudaGetLastError();
     return LLMOE_ERR_CUDA;
   }
-  if (dev >= 0 && dev < 64) g_smem_optin[dev][id] = (int)bytes;
+  if (cached) {
+    int cur = g_smem_optin[dev][id].load(std::memory_order_relaxed);
+    while (cur < (int)bytes && !g_smem_optin[dev][id].compare_exchange_weak(cur, (int)bytes)) {
+    }
+  }
   return LLMOE_SUCCESS;
 }
 
@@ -1330,24 +1344,32 @@ enum KernelId {
   kSignaledKernel = 6,
   kNumKernels = 7
 };
-int g_occupancy[64][32] = {{0}};
+// (dynamic shared memory bytes << 32 | resident CTAs per SM) of the last query
+std::atomic<uint64_t> g_occupancy[kMaxDevices][kMaxSlots];
 
 // Cache slot of a kernel instantiation: kernel id and payload type.
 int kslot(KernelId id, int dtype = 0) { return (int)id * 4 + dtype; }
+static_assert(kNumKernels * 4 <= kMaxSlots, "a cache slot per kernel and payload type");
 
-// Resident CTAs per SM of a kernel at kThreads threads and `smem` bytes,
-// cached per device.
+// Resident CTAs per SM of a kernel at `threads` threads and `smem` bytes of
+// dynamic shared memory, cached per device and kernel for the last size
+// asked (a kernel's threads are fixed; its shared memory follows the
+// geometry).
 int blocks_per_sm(int id, const void* fn, int threads, size_t smem) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-  if (dev < 64 && g_occupancy[dev][id] > 0) return g_occupancy[dev][id];
+  const bool cached = dev < kMaxDevices && smem < (1ull << 32);
+  if (cached) {
+    const uint64_t c = g_occupancy[dev][id].load(std::memory_order_relaxed);
+    if ((uint32_t)c > 0 && (c >> 32) == smem) return (int)(uint32_t)c;
+  }
   int n = 0;
   if (set_smem(id, fn, smem) != LLMOE_SUCCESS) return 1;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = 1;
   }
-  if (dev < 64) g_occupancy[dev][id] = n;
+  if (cached) g_occupancy[dev][id].store(((uint64_t)smem << 32) | (uint32_t)n, std::memory_order_relaxed);
   return n;
 }
 
@@ -1395,7 +1417,7 @@ static __device__ __align__(256) int32_t g_static_counters[kStaticMaxRanks];
 
 // The array's device address, looked up once per device (with that device
 // current): host code must not hand the symbol itself to a kernel.
-int32_t* g_static_counters_addr[64] = {nullptr};
+std::atomic<int32_t*> g_static_counters_addr[kMaxDevices];
 
 int static_counters(int32_t** out) {
   int dev = 0;
@@ -1403,16 +1425,19 @@ int static_counters(int32_t** out) {
     cudaGetLastError();
     return LLMOE_ERR_CUDA;
   }
-  if (dev < 64 && g_static_counters_addr[dev] != nullptr) {
-    *out = g_static_counters_addr[dev];
-    return LLMOE_SUCCESS;
+  if (dev < kMaxDevices) {
+    int32_t* c = g_static_counters_addr[dev].load(std::memory_order_acquire);
+    if (c != nullptr) {
+      *out = c;
+      return LLMOE_SUCCESS;
+    }
   }
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_static_counters) != cudaSuccess || p == nullptr) {
     cudaGetLastError();
     return LLMOE_ERR_CUDA;
   }
-  if (dev < 64) g_static_counters_addr[dev] = static_cast<int32_t*>(p);
+  if (dev < kMaxDevices) g_static_counters_addr[dev].store(static_cast<int32_t*>(p), std::memory_order_release);
   *out = static_cast<int32_t*>(p);
   return LLMOE_SUCCESS;
 }
