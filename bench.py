@@ -35,6 +35,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -99,11 +100,21 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source with comments and blank space removed (neither string
+    literal of the library holds a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_digest() -> str:
+    """Digest of the library's code (kernels and header), comments and layout
+    ignored: the traffic figures stay valid across comment-only edits."""
     h = hashlib.sha256()
     for rel in ("combine_routing_count_prefix_gb300/csrc/llmoe.cu", "include/llmoe.h"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

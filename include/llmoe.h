@@ -4,11 +4,12 @@
  *
  * One GPU holds R simulated expert-parallel ranks as R disjoint segments of
  * one device allocation ("rank buffers").  Each rank buffer has the layout of
- * LLMoEBufferLayout<bf16> from LL_MoE_Buffers.hpp (rocshmem LL_MoE example):
- * two buffer sets, each with a send region, a receive region and num_experts
- * int64 signal words; the combine roles alias the dispatch roles of the same
- * set.  Messages are one int32 header (the source token index) followed by
- * `hidden` bf16 values, 4 + 2 * hidden bytes, packed without padding.
+ * LLMoEBufferLayout<T> from LL_MoE_Buffers.hpp (rocshmem LL_MoE example) for
+ * a payload type T of bf16 (the default), fp16 or fp32: two buffer sets, each
+ * with a send region, a receive region and num_experts int64 signal words;
+ * the combine roles alias the dispatch roles of the same set.  Messages are
+ * one int32 header (the source token index) followed by `hidden` values of
+ * type T, 4 + hidden * sizeof(T) bytes, packed without padding.
  *
  * Conventions for every call:
  *   - All pointers passed to the data-path calls are DEVICE pointers into
@@ -70,7 +71,8 @@ typedef enum {
 #define LLMOE_DEV_DUPLICATE 2    /* one expert twice in one token's top-k */
 #define LLMOE_DEV_STALE_SIGNAL 3 /* a signal word was non-zero on entry (a clean was skipped) */
 #define LLMOE_DEV_SLOT_RANGE 4   /* a bucket overflowed num_max_tokens (only reachable with duplicates) */
-#define LLMOE_DEV_TIMEOUT 5      /* a bounded wait inside a kernel expired (a copy never completed) */
+#define LLMOE_DEV_TIMEOUT 5      /* a bounded wait inside a kernel expired (a copy never completed, or a
+                                    signal word was never raised) */
 #define LLMOE_DEV_BAD_MESSAGE 6  /* a staged-combine message header does not name its token */
 
 /* llmoe_buf_set_t.flags */
