@@ -713,6 +713,47 @@ def test_identity_expert_layer(L, name, dtype):
         assert not r.rb.signal_words(0).any(), "the combine zeroed the dispatch set's counts"
 
 
+@pytest.mark.parametrize("name,tokens", [("dsv3", 1), ("dsv3", 37), ("skewed", 0), ("many_small", 9)])
+def test_unpack_fewer_tokens_than_layout(L, name, tokens):
+    # a ragged call: num_tokens < num_max_tokens; rows still index with the
+    # layout's T, through both unpack kernels, the signalled dispatch and the
+    # identity-expert layer
+    w = WORKLOADS[name]
+    r = Round(L, w, seed=86 + tokens, tokens=tokens)
+    recv_x, recv_src = unpack_buffers(w)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch(r.x, r.idx, r.bs_d)
+    L.llmoe_unpack(recv_x, recv_src, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    r.check_dispatch()
+    u = oracle.unpack(r.inp["x"], r.inp["topk_idx"], w.E, num_max_tokens=w.T)
+    got_x, got_src = recv_x.cpu().numpy(), recv_src.cpu().numpy()
+    rows = u["rows"]
+    assert np.array_equal(got_x[rows].view(np.uint8), u["recv_x"][rows].view(np.uint8))
+    assert np.array_equal(got_src[rows], u["recv_src"][rows])
+    untouched = np.ones(got_src.shape[0], dtype=bool)
+    untouched[rows] = False
+    assert (got_src[untouched] == -7).all()
+    # the signalled dispatch on the same call
+    recv_x2, recv_src2 = unpack_buffers(w)
+    ws = torch.zeros(L.llmoe_signal_workspace_bytes(r.bs_d) // 4, dtype=torch.int32, device="cuda")
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch_signaled(r.x, r.idx, recv_x2, recv_src2, ws, 2_000_000_000, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    assert torch.equal(recv_src2, recv_src)
+    assert np.array_equal(recv_x2.cpu().numpy()[rows], got_x[rows])
+    # combine over the unpacked rows (identity experts)
+    L.llmoe_clean(r.bs_c)
+    L.llmoe_combine(recv_x, r.idx, r.wt, r.out, r.bs_c)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    ref, flags = oracle.combine(u["recv_x"], r.inp["topk_idx"], r.inp["topk_w"], w.H, w.E, num_max_tokens=w.T)
+    assert np.array_equal(r.out.cpu().numpy().view(np.uint16), ref)
+    assert np.array_equal(r.rb.signal_words(r.cs).cpu().numpy(), flags)
+
+
 def test_dispatch_signaled_times_out_without_signals(L):
     # completion counters that never reach the last CTA: no source ever
     # raises its signal words, so every consumer wait runs out
