@@ -188,6 +188,17 @@ __device__ __forceinline__ uint4 shift_words(const uint4& prev, const uint4& cur
   }
 }
 
+// 16-byte read-only load that does not allocate in L1: for rows read exactly
+// once (expert outputs in the combine and the staged put), where L1 lines
+// would only add allocation work to every miss.
+__device__ __forceinline__ uint4 ld_stream16(const uint4* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ void st16(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 __device__ __forceinline__ void st8(uint8_t* p, uint32_t a, uint32_t b) {
   *reinterpret_cast<uint2*>(p) = make_uint2(a, b);
@@ -609,7 +620,7 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
       for (int i = 0; i < kKBatch; ++i) {
         const int k = k0 + i;
         v[i] = make_uint4(0, 0, 0, 0);
-        if (k < g.K && rows[k] != nullptr) v[i] = __ldg(rows[k] + j);
+        if (k < g.K && rows[k] != nullptr) v[i] = ld_stream16(rows[k] + j);
       }
 #pragma unroll
       for (int i = 0; i < kKBatch; ++i) {
@@ -722,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 4) combine_put_kernel(Geometry g, co
 #pragma unroll
       for (int i = 0; i < kRowBatch; ++i) {
         const int j = (c + i) * 32 + lane;
-        cur[i] = (i < n && j < g.nq) ? __ldg(row + j) : make_uint4(0, 0, 0, 0);
+        cur[i] = (i < n && j < g.nq) ? ld_stream16(row + j) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int i = 0; i < kRowBatch; ++i) {
