@@ -455,6 +455,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     timed = max_over_ranks([sum(step_ms), wall], world)
     round_us = timed[0] / args.steps * 1e3
 
+    route = run_route(llmoe, w, idx, rb, tokens, flush)
     pipe = run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es)
     signaled = run_signaled(args, llmoe, w, x, idx, rb, es, flush)
 
@@ -514,6 +515,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                                "frac": round(algo["combine"] / c_us / 1e3 / peak, 4)},
             "combine_kernel_l2_flushed": {"us": round(cf_us, 3), "gbs": round(algo["combine"] / cf_us / 1e3, 1),
                                           "frac": round(algo["combine"] / cf_us / 1e3 / peak, 4)}}
+        line["route"] = route
         line["double_buffer"] = pipe
         line["dispatch_unpack"] = signaled
         if e2e is not None:
@@ -524,6 +526,31 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_route(llmoe, w, idx, rb, tokens, flush, steps: int = 200):
+    """llmoe_route on its own (the routing count / prefix scan that the
+    dispatch and combine kernels run inside): ids read, slots and counts
+    written; L2 flushed before each launch, events around it."""
+    import torch
+
+    slot = torch.empty((w.R, tokens, w.K), dtype=torch.int32, device="cuda")
+    counts = torch.empty((w.E, w.R), dtype=torch.int64, device="cuda")
+    bs = rb.buf_set(0, w.K)
+    cur = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps + 3):
+        flush()
+        if i >= 3:
+            evs[i - 3][0].record(cur)
+        llmoe.llmoe_route(idx, slot, counts, bs, cur)
+        if i >= 3:
+            evs[i - 3][1].record(cur)
+    torch.cuda.synchronize()
+    us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+    nbytes = idx.numel() * 8 + slot.numel() * 4 + counts.numel() * 8
+    return {"us": round(us, 3), "algorithmic_bytes": nbytes, "steps": steps,
+            "note": "events around llmoe_route alone, L2 flushed before each launch: launch- and latency-bound"}
 
 
 def run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es, micro_batches: int = 200):

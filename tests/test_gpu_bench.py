@@ -23,7 +23,7 @@ def test_bench_line_on_tiny():
     d = json.loads(lines[0])
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
                 "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks",
-                "kernels"):
+                "kernels", "route", "double_buffer", "dispatch_unpack"):
         assert key in d, key
     assert d["steps"] == 20 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["value"] > 0
     assert d["gpu_launches"] == 2 * d["steps"]
