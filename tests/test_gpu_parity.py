@@ -754,6 +754,22 @@ def test_unpack_fewer_tokens_than_layout(L, name, tokens):
     assert np.array_equal(r.rb.signal_words(r.cs).cpu().numpy(), flags)
 
 
+def test_unpack_more_buckets_than_the_balanced_prefix_holds(L):
+    # E * R = 16,384 buckets, beyond the balanced kernel's shared prefix
+    # (8,192), with more routed entries (65,536) than buckets: the per-bucket
+    # kernel runs although buckets hold several rows each
+    w = Workload("many_buckets", 2, 1024, 8, 8192, 32, mask_p=0.1)
+    r = Round(L, w, seed=87)
+    recv_x, recv_src = unpack_buffers(w)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch(r.x, r.idx, r.bs_d)
+    L.llmoe_unpack(recv_x, recv_src, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    r.check_dispatch()
+    check_unpack(r, recv_x, recv_src)
+
+
 def test_dispatch_signaled_times_out_without_signals(L):
     # completion counters that never reach the last CTA: no source ever
     # raises its signal words, so every consumer wait runs out
