@@ -847,6 +847,12 @@ __global__ void __launch_bounds__(kThreads, 4) combine_reduce_kernel(Geometry g,
 // warp finds the bucket of its first row by binary search and then walks its
 // range row by row (unpack_row).
 constexpr int kMaxScanBuckets = 8192;
+#ifndef LLMOE_UNPACK_THREADS
+#define LLMOE_UNPACK_THREADS 512
+#endif
+// Threads of a balanced-unpack CTA: every CTA reads and scans all the count
+// words, so fewer, larger CTAs read them fewer times for the same warps.
+constexpr int kUnpackThreads = LLMOE_UNPACK_THREADS;
 constexpr int kCountLoads = 8;  // count words a thread has in flight in the prologue
 
 __device__ __forceinline__ int find_bucket(const int* pre, int nb, int r) {
@@ -929,33 +935,34 @@ __device__ __forceinline__ void unpack_row(const Geometry& g, const uint8_t* msg
   }
 }
 
-__global__ void __launch_bounds__(kThreads, LLMOE_UNPACK_MIN_BLOCKS)
+__global__ void
+__launch_bounds__(kUnpackThreads, kUnpackThreads >= 1024 ? 1 : LLMOE_UNPACK_MIN_BLOCKS * 256 / kUnpackThreads)
     unpack_balanced_kernel(Geometry g, void* __restrict__ recv_x, int32_t* __restrict__ recv_src) {
   __shared__ int s_pre[kMaxScanBuckets];
-  __shared__ int s_part[kThreads / 32];
+  __shared__ int s_part[kUnpackThreads / 32];
   release_next_grid();
   wait_prior_grid();
   const int nb = g.E * g.R;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int b0 = 0; b0 < nb; b0 += kCountLoads * kThreads) {
+  for (int b0 = 0; b0 < nb; b0 += kCountLoads * kUnpackThreads) {
     int64_t c[kCountLoads];
 #pragma unroll
     for (int i = 0; i < kCountLoads; ++i) {
-      const int b = b0 + i * kThreads + tid, e = b / g.R, src = b - e * g.R;
+      const int b = b0 + i * kUnpackThreads + tid, e = b / g.R, src = b - e * g.R;
       c[i] = b < nb ? reinterpret_cast<const int64_t*>(g.base + (e / g.L) * g.rank_stride + g.sig_off)
                           [(int64_t)(e % g.L) * g.R + src]
                     : 0;
     }
 #pragma unroll
     for (int i = 0; i < kCountLoads; ++i) {
-      const int b = b0 + i * kThreads + tid;
+      const int b = b0 + i * kUnpackThreads + tid;
       if (b < nb) s_pre[b] = (int)max((int64_t)0, min(c[i], (int64_t)g.T_max));
     }
   }
   __syncthreads();
   // exclusive prefix: each thread scans a contiguous segment, the segment
   // totals are scanned across the block
-  const int seg = (nb + kThreads - 1) / kThreads, lo = min(nb, tid * seg), hi = min(nb, lo + seg);
+  const int seg = (nb + kUnpackThreads - 1) / kUnpackThreads, lo = min(nb, tid * seg), hi = min(nb, lo + seg);
   int sum = 0;
   for (int b = lo; b < hi; ++b) sum += s_pre[b];
   int incl = sum;
@@ -969,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, LLMOE_UNPACK_MIN_BLOCKS)
   int warp_base = 0;
   for (int w = 0; w < warp; ++w) warp_base += s_part[w];
   int total = 0;
-  for (int w = 0; w < kThreads / 32; ++w) total += s_part[w];
+  for (int w = 0; w < kUnpackThreads / 32; ++w) total += s_part[w];
   int run = warp_base + incl - sum;
   __syncthreads();  // every segment read its counts before any is overwritten
   for (int b = lo; b < hi; ++b) {
@@ -981,8 +988,8 @@ __global__ void __launch_bounds__(kThreads, LLMOE_UNPACK_MIN_BLOCKS)
 
   // the warp's contiguous range [ubeg, uend) of (row, chunk) units
   const int64_t nunits = (int64_t)total * g.nchunks;
-  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
-  const int64_t gw = ((int64_t)blockIdx.x * kThreads + tid) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kUnpackThreads) >> 5;
+  const int64_t gw = ((int64_t)blockIdx.x * kUnpackThreads + tid) >> 5;
   const int64_t per = (nunits + nwarps - 1) / nwarps;
   const int64_t ubeg = min(nunits, gw * per), uend = min(nunits, ubeg + per);
   if (ubeg >= uend) return;
@@ -1595,8 +1602,8 @@ int llmoe_unpack(void* recv_x, int32_t* recv_src, const llmoe_buf_set_t* bs, llm
   if (nb <= kMaxScanBuckets && nb < entries) {
     // one full wave: the copy is latency-bound, so every resident warp helps
     const int64_t wave = (int64_t)num_sms() * blocks_per_sm(kslot(kUnpackKernel, 1),
-                                                            (const void*)unpack_balanced_kernel, kThreads, 0);
-    return launch(unpack_balanced_kernel, (unsigned)wave, kThreads, 0, stream, g, recv_x, recv_src);
+                                                            (const void*)unpack_balanced_kernel, kUnpackThreads, 0);
+    return launch(unpack_balanced_kernel, (unsigned)wave, kUnpackThreads, 0, stream, g, recv_x, recv_src);
   }
   const int64_t wave =
       (int64_t)num_sms() * blocks_per_sm(kslot(kUnpackKernel), (const void*)unpack_kernel, kThreads, 0);
