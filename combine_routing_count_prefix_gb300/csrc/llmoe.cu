@@ -1055,6 +1055,98 @@ __device__ __forceinline__ void st_release_gpu(long long* p, long long v) {
   asm volatile("st.release.gpu.global.s64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Rank e / L's signal word le * R + src: the recv count of bucket (e, src).
+__device__ __forceinline__ long long* signal_word(const Geometry& g, int e, int src) {
+  return reinterpret_cast<long long*>(g.base + (e / g.L) * g.rank_stride + g.sig_off) + ((int64_t)(e % g.L) * g.R + src);
+}
+
+// Consumer work of the signalled dispatch for source rank s by this CTA,
+// member k of the Gs CTAs serving s.  The CTA's threads wait (bounded) for
+// s's signal words in parallel, scan the counts into s_pre (E ints of shared
+// memory) and split s's received (row, chunk) units evenly over the Gs * 8
+// warps.  Returns early, after reporting LLMOE_DEV_TIMEOUT, when a word of s
+// is not raised within the spin limit.  Called by every thread of the CTA.
+__device__ void consume_source(const Geometry& g, int s, int k, int Gs, int* s_pre, int* s_part, int* s_ok,
+                               void* __restrict__ recv_x, int32_t* __restrict__ recv_src, long long spin_limit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __syncthreads();  // s_pre / s_ok of the previous use have been read
+  if (tid == 0) *s_ok = 1;
+  __syncthreads();
+  for (int e = tid; e < g.E; e += kThreads) {
+    const long long* w = signal_word(g, e, s);
+    long long v = ld_acquire_gpu(w);
+    const long long start = clock64();
+    while (v == 0 && clock64() - start <= spin_limit) {
+      __nanosleep(64);
+      v = ld_acquire_gpu(w);
+    }
+    s_pre[e] = v < 0 ? (int)min(-v - 1, (long long)g.T_max) : 0;
+    if (v >= 0) *s_ok = 0;  // never raised (or not a raised signal)
+  }
+  __syncthreads();  // every count, and every thread's acquire, before any read of s's rows
+  if (*s_ok == 0) {
+    if (tid == 0) report(g.err, LLMOE_DEV_TIMEOUT);
+    return;
+  }
+  // exclusive prefix of the counts (each thread a contiguous segment)
+  const int seg = (g.E + kThreads - 1) / kThreads, lo = min(g.E, tid * seg), hi = min(g.E, lo + seg);
+  int sum = 0;
+  for (int e = lo; e < hi; ++e) sum += s_pre[e];
+  int incl = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) s_part[warp] = incl;
+  __syncthreads();
+  int run = incl - sum, total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) run += s_part[w];
+    total += s_part[w];
+  }
+  __syncthreads();  // every segment read its counts before any is overwritten
+  for (int e = lo; e < hi; ++e) {
+    const int ce = s_pre[e];
+    s_pre[e] = run;
+    run += ce;
+  }
+  __syncthreads();
+
+  // this warp's range [ubeg, uend) of s's (row, chunk) units
+  const int64_t nunits = (int64_t)total * g.nchunks;
+  const int64_t ws = (int64_t)Gs * (kThreads / 32), wi = (int64_t)k * (kThreads / 32) + warp;
+  const int64_t per = (nunits + ws - 1) / ws;
+  const int64_t ubeg = min(nunits, wi * per), uend = min(nunits, ubeg + per);
+  if (ubeg >= uend) return;
+  int r = (int)(ubeg / g.nchunks);
+  int c = (int)(ubeg - (int64_t)r * g.nchunks);
+  int64_t left = uend - ubeg;
+  int e = find_bucket(s_pre, g.E, r);
+  auto end_of = [&](int ex) { return ex + 1 < g.E ? s_pre[ex + 1] : total; };
+  int slot = r - s_pre[e];
+  while (left > 0) {
+    while (slot >= end_of(e) - s_pre[e]) {  // past this expert's rows: the next expert with rows
+      slot = 0;
+      ++e;
+    }
+    const int le = e % g.L;
+    const uint8_t* msg = g.base + (e / g.L) * g.rank_stride + g.recv_off +
+                         (((uint64_t)le * g.R + s) * g.T_max + slot) * g.msg;
+    const int64_t orow = ((int64_t)e * g.R + s) * g.T_max + slot;
+    const int cend = (int)min((int64_t)g.nchunks, c + left);  // this row's chunks in the range
+    const bool head = (c == 0);
+    int hv = 0;
+    if (head && lane == 0) hv = __ldcg(reinterpret_cast<const int32_t*>(msg));
+    left -= cend - c;
+    unpack_row<true>(g, msg, reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(recv_x) + orow * g.row_bytes), c,
+                     cend, lane);
+    if (head && lane == 0) recv_src[orow] = hv;
+    c = 0;
+    ++slot;
+  }
+}
+
 // Cooperative: every CTA is resident, so a consumer that waits on a signal
 // word only waits for producers that are running.  Producer work (CTA =
 // source rank src, token block) is the dispatch; the CTA that completes a
@@ -1066,13 +1158,11 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_signaled_kernel(Geometry
                                                                         const int64_t* __restrict__ idx,
                                                                         void* __restrict__ recv_x,
                                                                         int32_t* __restrict__ recv_src,
-                                                                        int32_t* __restrict__ done, long long spin_limit,
-                                                                        int warp_buckets) {
+                                                                        int32_t* __restrict__ done, long long spin_limit) {
   extern __shared__ __align__(128) unsigned char smem[];
   const RouteSmem s = carve_route(smem, g);
   uintptr_t* s_dst = reinterpret_cast<uintptr_t*>(s.slot + g.TB * g.K + (g.E & 1));
   __shared__ int s_last;
-  __shared__ long long s_word[kThreads / 32];
 
   const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
@@ -1132,45 +1222,48 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_signaled_kernel(Geometry
     if (threadIdx.x == 0) done[src] = 0;  // ready for the next call
   }
 
-  // ---- consumer.  warp_buckets: one warp per bucket (e, bsrc), round robin
-  // over the grid's warps (few rows per bucket); else one CTA per bucket,
-  // round robin over the CTAs, the bucket's rows round robin over its warps
-  // (a hot bucket is spread)
-  const int64_t nbuckets = (int64_t)g.E * g.R;
-  const int64_t first = warp_buckets ? ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5 : blockIdx.x;
-  const int64_t step = warp_buckets ? ((int64_t)gridDim.x * kThreads) >> 5 : gridDim.x;
-  for (int64_t bucket = first; bucket < nbuckets; bucket += step) {
-    const int e = (int)(bucket / g.R), bsrc = (int)(bucket % g.R), dst = e / g.L, le = e % g.L;
-    uint8_t* rank = g.base + dst * g.rank_stride;
-    long long* word = reinterpret_cast<long long*>(rank + g.sig_off) + ((int64_t)le * g.R + bsrc);
-    const bool waiter = warp_buckets ? lane == 0 : threadIdx.x == 0;
-    if (!warp_buckets) __syncthreads();  // s_word of the previous bucket has been read
-    long long v = 0;
-    if (waiter) {
-      v = ld_acquire_gpu(word);
-      const long long start = clock64();
-      while (v == 0 && clock64() - start <= spin_limit) {
-        __nanosleep(64);
-        v = ld_acquire_gpu(word);
+  // ---- consumer: CTAs grouped by source rank (consume_source).  Consumers
+  // do not rewrite the words: the last CTA to finish turns every raised word
+  // back into its plain count.
+  __shared__ int s_part[kThreads / 32];
+  __shared__ int s_ok;
+  if ((int)gridDim.x >= g.R) {
+    const int sg = blockIdx.x % g.R;
+    consume_source(g, sg, blockIdx.x / g.R, ((int)gridDim.x - sg + g.R - 1) / g.R, s.hist, s_part, &s_ok, recv_x,
+                   recv_src, spin_limit);
+  } else {
+    for (int sg = blockIdx.x; sg < g.R; sg += gridDim.x)
+      consume_source(g, sg, 0, 1, s.hist, s_part, &s_ok, recv_x, recv_src, spin_limit);
+  }
+  __syncthreads();  // the CTA's consumers are done
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's reads of the signal words before its completion count
+    s_last = atomicAdd(&done[g.R], 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    constexpr int kBatch = 8;  // words a thread has in flight at once
+    const int nw = g.E * g.R;
+    for (int i0 = 0; i0 < nw; i0 += kThreads * kBatch) {
+      long long* w[kBatch];
+      long long v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * kThreads + threadIdx.x;
+        w[j] = nullptr;
+        v[j] = 0;
+        if (i < nw) {
+          const int e = i / g.R;
+          w[j] = signal_word(g, e, i - e * g.R);
+          v[j] = __ldcg(w[j]);
+        }
       }
-      if (v == 0) report(g.err, LLMOE_DEV_TIMEOUT);
-      s_word[warp_buckets ? warp : 0] = v;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (v[j] < 0) *w[j] = -v[j] - 1;  // the plain count, as a dispatch leaves it
     }
-    // the bucket's readers come after the waiter's acquire
-    if (warp_buckets) __syncwarp(); else __syncthreads();
-    v = s_word[warp_buckets ? warp : 0];
-    if (v >= 0) continue;  // timed out (0), or not a raised signal: leave the bucket
-    const int cnt = (int)min(-v - 1, (long long)g.T_max);
-    const uint8_t* msg0 = rank + g.recv_off + ((uint64_t)le * g.R + bsrc) * g.T_max * g.msg;
-    uint8_t* row0 = reinterpret_cast<uint8_t*>(recv_x) + bucket * g.T_max * g.row_bytes;
-    for (int slot = warp_buckets ? 0 : warp; slot < cnt; slot += warp_buckets ? 1 : kThreads / 32) {
-      const uint8_t* msg = msg0 + (size_t)slot * g.msg;
-      int hv = 0;
-      if (lane == 0) hv = __ldcg(reinterpret_cast<const int32_t*>(msg));
-      unpack_row<true>(g, msg, reinterpret_cast<uint4*>(row0 + (size_t)slot * g.row_bytes), 0, g.nchunks, lane);
-      if (lane == 0) recv_src[bucket * g.T_max + slot] = hv;
-    }
-    if (waiter) *word = -v - 1;  // the plain count, as a dispatch leaves it
+    if (threadIdx.x == 0) done[g.R] = 0;  // ready for the next call
   }
 }
 
@@ -1431,7 +1524,7 @@ int launch(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
 // allocates.  Every GPU that loads the library holds it until the process
 // exits; every call on a device shares it.
 constexpr int kStaticMaxRanks = LLMOE_STATIC_MAX_RANKS;
-static __device__ __align__(256) int32_t g_static_counters[kStaticMaxRanks];
+static __device__ __align__(256) int32_t g_static_counters[kStaticMaxRanks + 1];  // per source, plus the consumers'
 
 // The array's device address, looked up once per device (with that device
 // current): host code must not hand the symbol itself to a kernel.
@@ -1613,7 +1706,7 @@ int llmoe_unpack(void* recv_x, int32_t* recv_src, const llmoe_buf_set_t* bs, llm
 
 size_t llmoe_signal_workspace_bytes(const llmoe_buf_set_t* bs) {
   if (bs == nullptr || bs->num_ranks < 1) return 0;
-  return ((size_t)bs->num_ranks * sizeof(int32_t) + 255) / 256 * 256;
+  return ((size_t)(bs->num_ranks + 1) * sizeof(int32_t) + 255) / 256 * 256;  // per source, plus the consumers'
 }
 
 int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src, void* workspace,
@@ -1649,11 +1742,8 @@ int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, void* recv_x
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // consumers as llmoe_unpack: a warp per bucket when there are at least as
-  // many buckets as routed entries, else a CTA per bucket
-  const int warp_buckets = (int64_t)g.E * g.R >= (int64_t)g.R * g.T * g.K;
   if (cudaLaunchKernelEx(&cfg, dispatch_signaled_kernel, g, x, topk_idx, recv_x, recv_src,
-                         static_cast<int32_t*>(workspace), (long long)spin_limit, warp_buckets) != cudaSuccess) {
+                         static_cast<int32_t*>(workspace), (long long)spin_limit) != cudaSuccess) {
     cudaGetLastError();
     return LLMOE_ERR_CUDA;
   }
@@ -1669,7 +1759,8 @@ int llmoe_dispatch_signaled_static(const void* x, const int64_t* topk_idx, void*
   if (rc != LLMOE_SUCCESS) return rc;
   // the counters must start at zero; a previous call may have left them
   // otherwise (a timeout), so clear the part this call uses, in stream order
-  if (cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)bs->num_ranks, (cudaStream_t)stream) != cudaSuccess) {
+  if (cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)(bs->num_ranks + 1), (cudaStream_t)stream) !=
+      cudaSuccess) {
     cudaGetLastError();
     return LLMOE_ERR_CUDA;
   }

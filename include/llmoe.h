@@ -239,7 +239,7 @@ LLMOE_API int llmoe_unpack(void* recv_x, int32_t* recv_src, const llmoe_buf_set_
 
 /* Bytes of the workspace llmoe_dispatch_signaled needs for this geometry.
  * No counterpart in the layout header: it holds one completion counter per
- * source rank. */
+ * source rank (producers) and one for the consumers. */
 LLMOE_API size_t llmoe_signal_workspace_bytes(const llmoe_buf_set_t* bs);
 
 /* Dispatch and unpack in one cooperative launch whose CTAs signal each other
@@ -248,17 +248,18 @@ LLMOE_API size_t llmoe_signal_workspace_bytes(const llmoe_buf_set_t* bs);
  * its wait returns: mscclpp.h, mscclppDevConn put / signal / wait).
  * Producer work is the dispatch of llmoe_dispatch.  When every CTA of a
  * source rank has written its rows, the last one writes that source's
- * signal words as -(count + 1).  Consumer work (the buckets of every
- * destination rank, spread over the same CTAs) waits for each bucket's signal
- * word to become non-zero, then unpacks it as llmoe_unpack does and rewrites
- * the word to the plain count.  The result is that of llmoe_dispatch followed
- * by llmoe_unpack.
+ * signal words as -(count + 1).  Consumer work runs on the same CTAs, its
+ * warps grouped by source rank: a warp of source s waits for every signal
+ * word of s to become non-zero, then unpacks an equal share of s's received
+ * rows as llmoe_unpack does.  The last warp to finish rewrites every raised
+ * word to the plain count.  The result is that of llmoe_dispatch followed by
+ * llmoe_unpack.
  *   workspace   device memory of llmoe_signal_workspace_bytes(bs) bytes,
  *               zero before the first call; each completed call leaves it
  *               zero.  After an LLMOE_DEV_TIMEOUT, zero it again.
  *   spin_limit  clock cycles a consumer waits for one signal word before it
  *               records LLMOE_DEV_TIMEOUT (needs bs->err) and skips that
- *               bucket; about 2e9 is one second at 2 GHz.  Unlike the
+ *               source; about 2e9 is one second at 2 GHz.  Unlike the
  *               unbounded waits of mscclpp.h, no wait here can hang.
  * Returns LLMOE_ERR_INVALID_ARGUMENT when the grid this geometry needs cannot
  * be resident all at once (the signalling needs every CTA running). */
@@ -275,9 +276,10 @@ LLMOE_API int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, vo
  * call: a plugin handed only raw device pointers by a host framework that
  * owns every allocation, or a latency-critical loop in which a cudaMalloc,
  * which may synchronize the device, is not acceptable.  This call needs no
- * workspace from them: the per-source completion counters live in a fixed
- * device array inside the library, sized for LLMOE_STATIC_MAX_RANKS ranks
- * (4 KB, held by every GPU that loads the library until the process exits).
+ * workspace from them: the completion counters (one per source, one for the
+ * consumers) live in a fixed device array inside the library, sized for
+ * LLMOE_STATIC_MAX_RANKS ranks (about 4 KB, held by every GPU that loads the
+ * library until the process exits).
  * It allocates nothing and calls no allocating routine.
  *   - Same arguments and result as llmoe_dispatch_signaled, minus the
  *     workspace.  num_ranks above LLMOE_STATIC_MAX_RANKS returns
