@@ -27,11 +27,13 @@
 //     in ascending k (__fmul_rn / __fadd_rn: never contracted to an FMA), the
 //     sum stored as T (bf16 / fp16 rounded to nearest even).
 //   combine_put_kernel, combine_reduce_kernel<T>: the staged combine through
-//     the combine receive buffers (messages realigned on write and on read).
+//     the combine receive buffers (messages written with realigned stores,
+//     read at their own 4-byte alignment).
 //   unpack_balanced_kernel, unpack_kernel: received messages to the experts'
 //     input layout, driven by the count words.
 //   dispatch_signaled_kernel: dispatch and unpack in one cooperative launch;
-//     CTAs signal each other through the count words, with bounded waits.
+//     producers raise each source's count words, consumer CTAs grouped by
+//     source wait for them (bounded) and unpack an equal share of its rows.
 //   clean_kernel: zeroes a set's R * E signal words (LLMoEBuffer::clean_meta).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
