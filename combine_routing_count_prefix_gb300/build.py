@@ -16,6 +16,9 @@ SRC = os.path.join(PKG, "csrc", "llmoe.cu")
 HDR = os.path.join(ROOT, "include", "llmoe.h")
 OUT_DIR = os.path.join(PKG, "_build")
 SO = os.path.join(OUT_DIR, "libllmoe.so")
+# the phase-trace build (-DLLMOE_PHASE_TRACE=1): the same library with per-CTA
+# timer stamps in the dispatch and combine kernels, for phase_budget.py only
+TRACE_SO = os.path.join(OUT_DIR, "libllmoe_trace.so")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -31,18 +34,23 @@ def nvcc() -> str:
     return cand
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Compile the library (or, with trace=True, its phase-trace build) unless
+    it is newer than its sources; returns the path of the shared object."""
+    out = TRACE_SO if trace else SO
     os.makedirs(OUT_DIR, exist_ok=True)
     newest = max(os.path.getmtime(SRC), os.path.getmtime(HDR))
-    if not force and os.path.exists(SO) and os.path.getmtime(SO) >= newest:
-        return SO
-    tmp = f"{SO}.{os.getpid()}.tmp"
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= newest:
+        return out
+    tmp = f"{out}.{os.getpid()}.tmp"
     cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), "-o", tmp, SRC]
+    if trace:
+        cmd.insert(1, "-DLLMOE_PHASE_TRACE=1")
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.run(cmd, check=True)
-    os.replace(tmp, SO)
-    return SO
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -73,6 +73,37 @@ __device__ __forceinline__ void report(int32_t* err, int32_t code) {
   if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// Phase trace, compiled in only with -DLLMOE_PHASE_TRACE=1 (a separate build
+// of the library; the normal build has none of it).  A traced kernel stamps
+// the global nanosecond timer and its SM's cycle counter at fixed points of
+// its prologue and data phase into a per-CTA row of a device array, which
+// llmoe_phase_trace_read copies out.  Used to find where a kernel's fixed
+// latency goes.
+#ifndef LLMOE_PHASE_TRACE
+#define LLMOE_PHASE_TRACE 0
+#endif
+#if LLMOE_PHASE_TRACE
+constexpr int kTraceCtas = 8192;
+constexpr int kTracePhases = 8;  // per CTA: kTracePhases timer stamps, kTracePhases cycle stamps
+__device__ unsigned long long g_phase_trace[kTraceCtas * 2 * kTracePhases];
+__device__ __forceinline__ void trace_phase(int p) {
+  if (blockIdx.x < kTraceCtas) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+    g_phase_trace[(size_t)blockIdx.x * 2 * kTracePhases + p] = t;
+    g_phase_trace[(size_t)blockIdx.x * 2 * kTracePhases + kTracePhases + p] = (unsigned long long)clock64();
+  }
+}
+#define TRACE(p, cond)           \
+  do {                           \
+    if (cond) trace_phase(p);    \
+  } while (0)
+#else
+#define TRACE(p, cond) \
+  do {                 \
+  } while (0)
+#endif
+
 // Programmatic dependent launch: every kernel here is launched so that it may
 // start while the previous kernel on the stream drains.  Each kernel first
 // lets the next kernel on the stream begin launching (that kernel still waits
@@ -101,20 +132,30 @@ __device__ __forceinline__ RouteSmem carve_route(unsigned char* smem, const Geom
 // Routing count / prefix scan for tokens [t0, t1) of source rank src, in two
 // steps.  route_hist loads the block's entries into s.ent and builds s.hist =
 // per-expert entries of the tokens before the block (returns after a
-// __syncthreads).  route_slot(q) then gives entry q's slot: hist[e] plus the
+// barrier).  route_slot(q) then gives entry q's slot: hist[e] plus the
 // earlier in-block tokens choosing e; each thread calls it for its own
 // entries, so a kernel can turn slots into addresses in the same pass.
 // route_count_block adds the block's entries to s.hist (full counts, for the
 // CTA of a source rank's last block); its caller syncs before reading them.
-constexpr int kPrefetch = 4;  // prefix ids each thread loads before the first barrier
+// route_hist runs on threads [0, nthr) of the CTA numbered by tid, which meet
+// at Sync() (a __syncthreads, or a named barrier of a subset of warps).
+//
+// Every CTA of a launch runs this prologue at the same moment, so its cost is
+// the instructions all their warps issue as much as its latency: one
+// shared-memory atomic per id, kPrefetch ids in flight per thread (one memory
+// round trip for up to kPrefetch * nthr ids), and the per-entry slot work on
+// one thread per entry.
+constexpr int kPrefetch = 8;  // prefix ids a thread has in flight per pass
 
+__device__ __forceinline__ void sync_all() { __syncthreads(); }
+
+template <void (*Sync)() = sync_all>
 __device__ void route_hist(const Geometry& g, const int64_t* __restrict__ idx, int src, int t0, int t1,
-                           const RouteSmem& s) {
-  const int tid = threadIdx.x, nthr = blockDim.x;
+                           const RouteSmem& s, int tid, int nthr) {
   const int K = g.K, E = g.E;
   const int64_t* src_idx = idx + (int64_t)src * g.T * K;
   const int npre = t0 * K, nblock = (t1 - t0) * K;
-  // issue the prefix loads first: one memory latency for the whole prologue
+  // the first pass of prefix loads is issued before anything else
   int64_t pre[kPrefetch];
 #pragma unroll
   for (int j = 0; j < kPrefetch; ++j) {
@@ -127,15 +168,20 @@ __device__ void route_hist(const Geometry& g, const int64_t* __restrict__ idx, i
     s.ent[q] = (e >= 0 && e < E) ? (int)e : -1;
     if (e < -1 || e >= E) report(g.err, LLMOE_DEV_BAD_EXPERT);
   }
-  __syncthreads();
+  Sync();
+  for (int base = 0;;) {
 #pragma unroll
-  for (int j = 0; j < kPrefetch; ++j)
-    if (pre[j] >= 0 && pre[j] < E) atomicAdd(&s.hist[pre[j]], 1);
-  for (int i = tid + kPrefetch * nthr; i < npre; i += nthr) {
-    const int64_t e = src_idx[i];
-    if (e >= 0 && e < E) atomicAdd(&s.hist[e], 1);
+    for (int j = 0; j < kPrefetch; ++j)
+      if (pre[j] >= 0 && pre[j] < E) atomicAdd(&s.hist[pre[j]], 1);
+    base += kPrefetch * nthr;
+    if (base >= npre) break;
+#pragma unroll
+    for (int j = 0; j < kPrefetch; ++j) {
+      const int i = base + tid + j * nthr;
+      pre[j] = i < npre ? src_idx[i] : -1;
+    }
   }
-  __syncthreads();
+  Sync();
 }
 
 __device__ __forceinline__ int route_slot(const Geometry& g, const RouteSmem& s, int q) {
@@ -160,16 +206,19 @@ __device__ __forceinline__ void route_count_block(const RouteSmem& s, int nblock
     if (s.ent[q] >= 0) atomicAdd(&s.hist[s.ent[q]], 1);
 }
 
-// LLMOE_FLAG_CLEAN_OTHER_SET: the grid zeroes the other buffer set's R * E
-// signal words (the clean that the next call on that set needs), after it
-// has waited for the previous kernel.
-__device__ __forceinline__ void clean_other_set(const Geometry& g) {
+// Zeroes the other buffer set's R * E signal words (LLMOE_FLAG_CLEAN_OTHER_SET:
+// the clean that the next call on that set needs), words first, first +
+// stride, ...; called after the kernel has waited for the previous one.
+__device__ __forceinline__ void clean_other_set(const Geometry& g, int64_t first, int64_t stride) {
   if ((g.flags & LLMOE_FLAG_CLEAN_OTHER_SET) == 0) return;
   const int64_t n = (int64_t)g.R * g.E;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t i = first; i < n; i += stride) {
     const int64_t r = i / g.E, e = i % g.E;
     reinterpret_cast<int64_t*>(g.base + r * g.rank_stride + g.other_sig_off)[e] = 0;
   }
+}
+__device__ __forceinline__ void clean_other_set(const Geometry& g) {
+  clean_other_set(g, blockIdx.x * (int64_t)blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
 }
 
 // Writes rank dst's (dispatch) or rank src's (combine) signal words from the
@@ -177,6 +226,29 @@ __device__ __forceinline__ void clean_other_set(const Geometry& g) {
 __device__ __forceinline__ void put_signal(const Geometry& g, int64_t* word, int value) {
   if (g.err != nullptr && *reinterpret_cast<volatile int64_t*>(word) != 0) report(g.err, LLMOE_DEV_STALE_SIGNAL);
   *word = (int64_t)value;
+}
+
+// The first R CTAs of a dispatch or combine grid are count CTAs, one per
+// source rank src: the per-expert counts of all of src's tokens (the
+// histogram of its ids) become the signal words (dispatch: rank e / L's word
+// (e % L) * R + src = the count of bucket (e, src); combine: rank src's word e
+// = rows expert e returns to src), and the count CTAs together zero the other
+// set's words when LLMOE_FLAG_CLEAN_OTHER_SET asks for it.  They move no rows,
+// so no data CTA carries the counts after its rows.
+__device__ void count_source(const Geometry& g, const int64_t* __restrict__ idx, int src, const RouteSmem& s,
+                             bool early, bool dispatch_words) {
+  release_next_grid();
+  if (!early) wait_prior_grid();
+  route_hist(g, idx, src, g.T, g.T, s, threadIdx.x, blockDim.x);  // all tokens: the full counts
+  if (early) wait_prior_grid();  // the signal words may be in use until now
+  clean_other_set(g, (int64_t)src * blockDim.x + threadIdx.x, (int64_t)g.R * blockDim.x);
+  for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
+    int64_t* w = dispatch_words
+                     ? reinterpret_cast<int64_t*>(g.base + (e / g.L) * g.rank_stride + g.sig_off) +
+                           ((int64_t)(e % g.L) * g.R + src)
+                     : reinterpret_cast<int64_t*>(g.base + src * g.rank_stride + g.sig_off) + e;
+    put_signal(g, w, s.hist[e]);
+  }
 }
 
 // Destination quad from the previous and current source quads when the
@@ -347,7 +419,19 @@ constexpr int kDspThreads = 32 * (1 + kDspConsumers);
 #endif
 constexpr int kDestRegs = LLMOE_DSP_DEST_REGS > 0 ? LLMOE_DSP_DEST_REGS : 1;  // destinations a dispatch thread keeps in registers
 
-__global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const void* __restrict__ x,
+// Named barrier of the consumer warps of a dispatch CTA (the producer warp
+// streams x and does not take part in the route scan).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kDspConsumers * 32) : "memory");
+}
+
+// Grid: R count CTAs (count_source), then R * nblk data CTAs, data CTA
+// (src, b) owning tokens [b * TB, b * TB + TB) of source rank src.  Warp 0
+// is the producer: its lane 0 streams the CTA's x rows into the ring from
+// the start.  The consumer warps meanwhile run the route scan among
+// themselves (named barrier) and pack the destinations into shared memory,
+// then take the ring's chunks.
+__global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, const void* __restrict__ x,
                                                                const int64_t* __restrict__ idx) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ring<kDspStages> ring;
@@ -358,14 +442,20 @@ __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const
   __shared__ RingState st;
   const RouteSmem s = carve_route(reinterpret_cast<unsigned char*>(ring.empty + kDspStages), g);
   uintptr_t* s_dst = reinterpret_cast<uintptr_t*>(s.slot + g.TB * g.K + (g.E & 1));
+  const bool early = (g.flags & LLMOE_FLAG_INPUTS_READY) != 0;
+  if ((int)blockIdx.x < g.R) {
+    count_source(g, idx, blockIdx.x, s, early, true);
+    return;
+  }
 
-  const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
+  const int bid = (int)blockIdx.x - g.R;
+  const int src = bid / g.nblk, b = bid % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
-  const bool last = (b == g.nblk - 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row_bytes = g.row_bytes;
   const int nch = (row_bytes + kDspChunk - 1) / kDspChunk;
   const int n_iters = (t1 - t0) * nch;
+  TRACE(0, threadIdx.x == 0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kDspStages; ++i) {
@@ -376,65 +466,61 @@ __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const
     st.issued = 0;
     st.consumed = INT_MAX;
   }
-  const bool early = (g.flags & LLMOE_FLAG_INPUTS_READY) != 0;
   release_next_grid();
   if (!early) wait_prior_grid();
-
-  // x does not depend on the routing: start streaming it before the scan
-  const uint8_t* xsrc = reinterpret_cast<const uint8_t*>(x) + ((int64_t)src * g.T + t0) * g.row_bytes;
-  auto issue = [&](int it) {
-    const int tl = it / nch, c = it % nch;
-    const int len = min(kDspChunk, row_bytes - c * kDspChunk);
-    uint8_t* dst = ring.stage(it % kDspStages);
-    const uint8_t* row = xsrc + (size_t)tl * row_bytes;
-    if (c == 0) {
-      mbar_arrive_expect_tx(&ring.full[it % kDspStages], len);
-      bulk_load(dst + 16, row, len, &ring.full[it % kDspStages]);
-    } else {
-      mbar_arrive_expect_tx(&ring.full[it % kDspStages], len + 16);
-      bulk_load(dst, row + c * kDspChunk - 16, len + 16, &ring.full[it % kDspStages]);
-    }
-  };
+  TRACE(1, threadIdx.x == 0);
   __syncthreads();  // barriers initialised
-  int next = 0;
-  if (threadIdx.x == 0)
-    for (; next < n_iters && next < kDspStages; ++next) issue(next);
-
-  route_hist(g, idx, src, t0, t1, s);
-  const int nblock = (t1 - t0) * g.K;
-  for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
-    const int e = s.ent[q], sl = route_slot(g, s, q);
-    uintptr_t d = 0;
-    if (sl >= 0) {
-      const int dst = e / g.L, le = e % g.L;
-      const uint64_t row = ((uint64_t)le * g.R + src) * g.T_max + sl;
-      d = pack_dest(g.base + dst * g.rank_stride + g.recv_off + row * g.msg);
-    }
-    s_dst[q] = d;
-  }
-  __syncthreads();
-  if (early) wait_prior_grid();  // the receive rows and signal words may be in use until now
-  clean_other_set(g);
-  if (last) route_count_block(s, nblock);
 
   if (warp == 0) {
+    // producer: x does not depend on the routing, so it streams from the start
     if (lane == 0) {
+      const uint8_t* xsrc = reinterpret_cast<const uint8_t*>(x) + ((int64_t)src * g.T + t0) * row_bytes;
+      int next = 0;
       for (; next < n_iters; ++next) {
-        const int use = next / kDspStages;
-        if (!mbar_wait(&ring.empty[next % kDspStages], (use - 1) & 1, g.err)) break;
-        issue(next);
+        const int sidx = next % kDspStages, use = next / kDspStages;
+        if (use > 0 && !mbar_wait(&ring.empty[sidx], (use - 1) & 1, g.err)) break;
+        const int tl = next / nch, c = next % nch;
+        const int len = min(kDspChunk, row_bytes - c * kDspChunk);
+        uint8_t* dst = ring.stage(sidx);
+        const uint8_t* row = xsrc + (size_t)tl * row_bytes;
+        if (c == 0) {
+          mbar_arrive_expect_tx(&ring.full[sidx], len);
+          bulk_load(dst + 16, row, len, &ring.full[sidx]);
+        } else {
+          mbar_arrive_expect_tx(&ring.full[sidx], len + 16);
+          bulk_load(dst, row + c * kDspChunk - 16, len + 16, &ring.full[sidx]);
+        }
       }
       st.issued = next;
     }
+    __syncwarp();  // the warp meets the CTA barrier below converged
   } else {
     const int ct = threadIdx.x - 32;  // the 16-byte quad of the chunk this thread moves
-    const bool small_k = LLMOE_DSP_DEST_REGS > 0 && g.K <= kDestRegs;
+    route_hist<consumers_sync>(g, idx, src, t0, t1, s, ct, kDspConsumers * 32);
+    TRACE(2, threadIdx.x == 32);
+    const int nblock = (t1 - t0) * g.K;
+    for (int q = ct; q < nblock; q += kDspConsumers * 32) {
+      const int e = s.ent[q], sl = route_slot(g, s, q);
+      uintptr_t d = 0;
+      if (sl >= 0) {
+        const int dst = e / g.L, le = e % g.L;
+        const uint64_t row = ((uint64_t)le * g.R + src) * g.T_max + sl;
+        d = pack_dest(g.base + dst * g.rank_stride + g.recv_off + row * g.msg);
+      }
+      s_dst[q] = d;
+    }
+    consumers_sync();
+    TRACE(3, threadIdx.x == 32);
+    if (early) wait_prior_grid();  // the receive rows may be in use until now
+    TRACE(4, threadIdx.x == 32);
+    const bool small_k = g.K <= kDestRegs;
     uintptr_t dreg[kDestRegs];  // top-k <= kDestRegs: the token's destinations, kept across its chunks
     int cached_tl = -1;
     int it = 0;
     for (; it < n_iters; ++it) {
       const int sidx = it % kDspStages;
       if (!mbar_wait(&ring.full[sidx], (it / kDspStages) & 1, g.err)) break;
+      TRACE(5, threadIdx.x == 32 && it == 0);
       const int tl = it / nch, c = it % nch;
       const int len = min(kDspChunk, row_bytes - c * kDspChunk);
       const uint8_t* sb = ring.stage(sidx);
@@ -464,18 +550,11 @@ __global__ void __launch_bounds__(kDspThreads) dispatch_kernel(Geometry g, const
       if (lane == 0) mbar_arrive(&ring.empty[sidx]);
     }
     if (lane == 0) atomicMin(&st.consumed, it);
+    TRACE(6, threadIdx.x == 32);
   }
   __syncthreads();
   if (st.consumed < st.issued) ring_drain(ring, st, g.err);
-
-  if (last) {
-    // rank dst's word le * R + src = count of bucket (le, src)
-    for (int e = threadIdx.x; e < g.E; e += blockDim.x) {
-      const int dst = e / g.L, le = e % g.L;
-      int64_t* w = reinterpret_cast<int64_t*>(g.base + dst * g.rank_stride + g.sig_off) + ((int64_t)le * g.R + src);
-      put_signal(g, w, s.hist[e]);
-    }
-  }
+  TRACE(7, threadIdx.x == 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -564,9 +643,10 @@ constexpr int kCmbThreads = LLMOE_CMB_THREADS;
 constexpr int kCmbWarps = kCmbThreads / 32;
 constexpr int kKBatch = 8;
 
-// One warp reduces 32 quads (512 B) of one output row per unit: up to
-// kKBatch expert rows are loaded (16 B per lane each) before they are
-// accumulated, in ascending k.
+// Grid: R count CTAs (count_source: the flag words), then R * nblk data CTAs.
+// A data CTA reduces tokens [t0, t1) of source rank src; one warp reduces 32
+// quads (512 B) of one output row per unit: up to kKBatch expert rows are
+// loaded (16 B per lane each) before they are accumulated, in ascending k.
 template <int DT>
 __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const void* __restrict__ y,
                                                               const int64_t* __restrict__ idx,
@@ -577,18 +657,25 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
   const int TBK = g.TB * g.K;
   const uint4** s_row = reinterpret_cast<const uint4**>(s.slot + TBK + (g.E & 1));
   float* s_w = reinterpret_cast<float*>(s_row + TBK);
+  const bool early = (g.flags & LLMOE_FLAG_INPUTS_READY) != 0;
+  if ((int)blockIdx.x < g.R) {
+    count_source(g, idx, blockIdx.x, s, early, false);
+    return;
+  }
 
-  const int src = blockIdx.x / g.nblk, b = blockIdx.x % g.nblk;
+  const int bid = (int)blockIdx.x - g.R;
+  const int src = bid / g.nblk, b = bid % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
-  const bool last = (b == g.nblk - 1);
   const int nblock = (t1 - t0) * g.K;
   const float* wblk = topk_w + ((int64_t)src * g.T + t0) * g.K;
-  const bool early = (g.flags & LLMOE_FLAG_INPUTS_READY) != 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  TRACE(0, threadIdx.x == 0);
   release_next_grid();
   if (!early) wait_prior_grid();
+  TRACE(1, threadIdx.x == 0);
   const float w0 = threadIdx.x < nblock ? wblk[threadIdx.x] : 0.0f;  // before the prologue's barriers
-
-  route_hist(g, idx, src, t0, t1, s);
+  route_hist(g, idx, src, t0, t1, s, threadIdx.x, blockDim.x);
+  TRACE(2, threadIdx.x == 0);
   for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
     const int e = s.ent[q], sl = route_slot(g, s, q);
     const uint4* r = nullptr;
@@ -600,11 +687,10 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
     s_w[q] = q == threadIdx.x ? w0 : wblk[q];
   }
   __syncthreads();
-  if (early) wait_prior_grid();  // y and the signal words may come from the previous kernel
-  clean_other_set(g);
-  if (last) route_count_block(s, nblock);
+  TRACE(3, threadIdx.x == 0);
+  if (early) wait_prior_grid();  // y may come from the previous kernel
+  TRACE(4, threadIdx.x == 0);
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nunits = (t1 - t0) * g.nchunks;
   for (int u = warp; u < nunits; u += kCmbWarps) {
     const int tl = u / g.nchunks, c = u % g.nchunks;
@@ -614,32 +700,28 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    const uint4* const* rows = s_row + tl * g.K;
-    const float* ws = s_w + tl * g.K;
+    const uint4* const* trows = s_row + tl * g.K;
+    const float* tws = s_w + tl * g.K;
     for (int k0 = 0; k0 < g.K; k0 += kKBatch) {
       uint4 v[kKBatch];
 #pragma unroll
       for (int i = 0; i < kKBatch; ++i) {
         const int k = k0 + i;
         v[i] = make_uint4(0, 0, 0, 0);
-        if (k < g.K && rows[k] != nullptr) v[i] = ld_stream16(rows[k] + j);
+        if (k < g.K && trows[k] != nullptr) v[i] = ld_stream16(trows[k] + j);
       }
 #pragma unroll
       for (int i = 0; i < kKBatch; ++i) {
         const int k = k0 + i;
-        if (k < g.K && rows[k] != nullptr) axpy_q<DT>(acc, ws[k], v[i]);
+        if (k < g.K && trows[k] != nullptr) axpy_q<DT>(acc, tws[k], v[i]);
       }
     }
     reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + ((int64_t)src * g.T + t) * g.row_bytes)[j] =
         pack_q<DT>(acc);
+    TRACE(5, threadIdx.x == 0 && u == warp);
   }
-
-  if (last) {
-    __syncthreads();
-    // rank src's word e = rows expert e returns to src
-    int64_t* w = reinterpret_cast<int64_t*>(g.base + src * g.rank_stride + g.sig_off);
-    for (int e = threadIdx.x; e < g.E; e += blockDim.x) put_signal(g, w + e, s.hist[e]);
-  }
+  TRACE(6, threadIdx.x == 0);
+  TRACE(7, threadIdx.x == 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -700,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 4) combine_put_kernel(Geometry g, co
   release_next_grid();
   if (!early) wait_prior_grid();
 
-  route_hist(g, idx, src, t0, t1, s);
+  route_hist(g, idx, src, t0, t1, s, threadIdx.x, blockDim.x);
   uint8_t* rbase = g.base + src * g.rank_stride + g.recv_off;
   for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
     const int e = s.ent[q], sl = route_slot(g, s, q);
@@ -1172,7 +1254,7 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_signaled_kernel(Geometry
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- producer: this CTA's rows
-  route_hist(g, idx, src, t0, t1, s);
+  route_hist(g, idx, src, t0, t1, s, threadIdx.x, blockDim.x);
   for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
     const int e = s.ent[q], sl = route_slot(g, s, q);
     uintptr_t d = 0;
@@ -1279,7 +1361,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(Geometry g, const int64
   const bool last = (b == g.nblk - 1);
   release_next_grid();
   wait_prior_grid();
-  route_hist(g, idx, src, t0, t1, s);
+  route_hist(g, idx, src, t0, t1, s, threadIdx.x, blockDim.x);
   const int nblock = (t1 - t0) * g.K;
   for (int q = threadIdx.x; q < nblock; q += blockDim.x)
     slot_out[((int64_t)src * g.T + t0) * g.K + q] = route_slot(g, s, q);
@@ -1412,11 +1494,13 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   return LLMOE_SUCCESS;
 }
 
-// Tokens per CTA: the fewest that keep the grid within one wave of resident
-// CTAs (SMs x blocks_per_sm), at most kMaxTokensPerBlock.
-void set_blocking(Geometry* g, int blocks_per_sm) {
+// Tokens per CTA: the fewest that keep the grid (plus extra_ctas other CTAs)
+// within one wave of resident CTAs (SMs x blocks_per_sm), at most
+// kMaxTokensPerBlock.
+void set_blocking(Geometry* g, int blocks_per_sm, int extra_ctas = 0) {
   const int64_t tokens = (int64_t)g->R * g->T;
-  const int64_t wave = (int64_t)num_sms() * (blocks_per_sm > 0 ? blocks_per_sm : 1);
+  int64_t wave = (int64_t)num_sms() * (blocks_per_sm > 0 ? blocks_per_sm : 1) - extra_ctas;
+  if (wave < 1) wave = 1;
   int64_t tb = (tokens + wave - 1) / wave;
   if (tb < 1) tb = 1;
   if (tb > kMaxTokensPerBlock) tb = kMaxTokensPerBlock;
@@ -1555,15 +1639,19 @@ int static_counters(int32_t** out) {
   return LLMOE_SUCCESS;
 }
 
+// Dispatch and combine grids: R count CTAs, then R * nblk data CTAs (none
+// when the call has no tokens).
+unsigned count_and_data_ctas(const Geometry& g) { return (unsigned)(g.R + (g.T > 0 ? g.R * g.nblk : 0)); }
+
 template <int DT>
 int launch_combine(Geometry& g, const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                    llmoe_stream_t stream) {
   const int id = kslot(kCombineKernel, DT);
-  set_blocking(&g, blocks_per_sm(id, (const void*)combine_kernel<DT>, kCmbThreads, combine_smem_bytes(g)));
+  set_blocking(&g, blocks_per_sm(id, (const void*)combine_kernel<DT>, kCmbThreads, combine_smem_bytes(g)), g.R);
   const size_t smem = combine_smem_bytes(g);
   const int rc = set_smem(id, (const void*)combine_kernel<DT>, smem);
   if (rc != LLMOE_SUCCESS) return rc;
-  return launch(combine_kernel<DT>, g.R * g.nblk, kCmbThreads, smem, stream, g, y, topk_idx, topk_w, out);
+  return launch(combine_kernel<DT>, count_and_data_ctas(g), kCmbThreads, smem, stream, g, y, topk_idx, topk_w, out);
 }
 
 template <int DT>
@@ -1574,6 +1662,27 @@ int launch_reduce(const Geometry& g, const int64_t* topk_idx, const float* topk_
   const int64_t blocks = std::min<int64_t>(wave, (warps + kThreads / 32 - 1) / (kThreads / 32));
   return launch(combine_reduce_kernel<DT>, (unsigned)blocks, kThreads, 0, stream, g, topk_idx, topk_w, out);
 }
+
+#if LLMOE_PHASE_TRACE
+// Reference kernels of the trace build, launched the way the data kernels
+// are: an empty one, and one whose single thread per CTA loads one cold word,
+// to time a launch and a cold load on their own.
+__global__ void trace_empty_kernel() {
+  release_next_grid();
+  wait_prior_grid();
+  TRACE(0, threadIdx.x == 0);
+}
+__global__ void trace_load_kernel(const int64_t* p, int64_t* out) {
+  release_next_grid();
+  wait_prior_grid();
+  TRACE(0, threadIdx.x == 0);
+  if (threadIdx.x == 0) {
+    const int64_t v = p[blockIdx.x * 4096];
+    TRACE(1, true);
+    out[blockIdx.x] = v;
+  }
+}
+#endif
 
 }  // namespace
 
@@ -1627,10 +1736,11 @@ int llmoe_dispatch(const void* x, const int64_t* topk_idx, const llmoe_buf_set_t
   if (rc != LLMOE_SUCCESS) return rc;
   if (g.T > 0 && (x == nullptr || topk_idx == nullptr || !aligned(x, 16) || !aligned(topk_idx, 8)))
     return LLMOE_ERR_INVALID_ARGUMENT;
-  set_blocking(&g, blocks_per_sm(kslot(kDispatchKernel), (const void*)dispatch_kernel, kDspThreads, dispatch_smem_bytes(g)));
+  set_blocking(&g, blocks_per_sm(kslot(kDispatchKernel), (const void*)dispatch_kernel, kDspThreads, dispatch_smem_bytes(g)),
+               g.R);
   const size_t smem = dispatch_smem_bytes(g);
   if ((rc = set_smem(kslot(kDispatchKernel), (const void*)dispatch_kernel, smem)) != LLMOE_SUCCESS) return rc;
-  return launch(dispatch_kernel, g.R * g.nblk, kDspThreads, smem, stream, g, x, topk_idx);
+  return launch(dispatch_kernel, count_and_data_ctas(g), kDspThreads, smem, stream, g, x, topk_idx);
 }
 
 int llmoe_combine(const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
@@ -1793,6 +1903,32 @@ int llmoe_get_error(const llmoe_buf_set_t* bs, llmoe_stream_t stream, int32_t* c
   *code = v;
   return LLMOE_SUCCESS;
 }
+
+#if LLMOE_PHASE_TRACE
+// Trace build only (not declared in llmoe.h): copy the per-CTA stamps of the
+// last traced launches out, clear them, and time the two reference kernels.
+LLMOE_API int llmoe_phase_trace_read(unsigned long long* host, int max_ctas) {
+  const int n = std::min(max_ctas, kTraceCtas);
+  if (host == nullptr || n < 1) return LLMOE_ERR_INVALID_ARGUMENT;
+  if (cudaMemcpyFromSymbol(host, g_phase_trace, sizeof(unsigned long long) * 2 * kTracePhases * (size_t)n) !=
+      cudaSuccess)
+    return LLMOE_ERR_CUDA;
+  return LLMOE_SUCCESS;
+}
+LLMOE_API int llmoe_phase_trace_clear(llmoe_stream_t stream) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_phase_trace) != cudaSuccess) return LLMOE_ERR_CUDA;
+  return cudaMemsetAsync(p, 0, sizeof(g_phase_trace), (cudaStream_t)stream) == cudaSuccess ? LLMOE_SUCCESS
+                                                                                            : LLMOE_ERR_CUDA;
+}
+LLMOE_API int llmoe_trace_empty(int ctas, llmoe_stream_t stream) {
+  return launch(trace_empty_kernel, (unsigned)ctas, kThreads, 0, stream);
+}
+// p: ctas * 4096 int64 words (one cold word 32 KB apart per CTA), out: ctas words
+LLMOE_API int llmoe_trace_load(const int64_t* p, int64_t* out, int ctas, llmoe_stream_t stream) {
+  return launch(trace_load_kernel, (unsigned)ctas, kThreads, 0, stream, p, out);
+}
+#endif
 
 const char* llmoe_status_string(int status) {
   switch (status) {

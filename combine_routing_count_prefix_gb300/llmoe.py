@@ -17,7 +17,10 @@ import os
 
 import torch
 
-_SO = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libllmoe.so")
+# LLMOE_LIBRARY selects another build of the same library (the phase-trace
+# build of phase_budget.py); by default the in-tree libllmoe.so
+_SO = os.environ.get("LLMOE_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build",
+                                                       "libllmoe.so")
 if not os.path.exists(_SO):
     raise ImportError(f"{_SO} is missing: build it with combine_routing_count_prefix_gb300.build.build()")
 _lib = ctypes.CDLL(_SO)

@@ -1,0 +1,200 @@
+"""Where a dispatch or combine launch spends its time: a phase budget.
+
+Builds the phase-trace variant of the library (-DLLMOE_PHASE_TRACE=1: the
+same kernels with timer stamps at fixed points of every CTA's prologue and
+data phase), runs each kernel alone after the bench's L2 flush, and prints
+per workload, in microseconds:
+
+- the kernel as CUDA events see it (launch, run, drain);
+- the span from the first CTA's entry to the last CTA's exit (globaltimer);
+- for each phase, the time from a CTA's own entry to that phase: median and
+  maximum over the CTAs, median over steps;
+- when the CTAs entered and left, relative to the first CTA's entry;
+- two reference kernels launched the same way: an empty one, and one whose
+  single thread per CTA loads one word (its stamps give the load latency).
+
+Each kernel is measured after the bench's L2 flush ("flush"), after the
+flush and a call of the same kernel on a tiny separate problem, which brings
+the kernel's code back into L2 but none of this call's data ("warm-code"),
+and back to back ("no-flush").
+
+Usage (one GPU):
+    python -m combine_routing_count_prefix_gb300.phase_budget [--workloads tiny,many_small,dsv3] [--steps 30]
+
+The stamps themselves cost a few global stores per CTA; the normal build has
+none of them.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import statistics
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PHASES = {
+    "dispatch": ["entry", "prior grid done", "route histogram built (consumer warps)", "destinations packed",
+                 "consumers start (after the early wait)", "first chunk in shared memory", "consumer warp done",
+                 "exit"],
+    "combine": ["entry", "prior grid done (not early)", "route histogram built", "row table ready",
+                "prior grid done (early)", "first unit stored", "all units stored", "exit"],
+}
+NPH = 8  # stamps per CTA and kind (globaltimer, then clock64)
+SM_MHZ = 2070  # the GB300's maximum SM clock, for the cycle stamps
+FLUSH_BYTES = 512 << 20
+FLUSH_READ_BYTES = 256 << 20
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--workloads", default="tiny,many_small,skewed,dsv3")
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--modes", default="flush,warm-code,no-flush")
+    args = ap.parse_args(argv)
+
+    from combine_routing_count_prefix_gb300 import build as cuda_build
+
+    # LLMOE_TRACE_LIBRARY: an already built trace library (e.g. a variant
+    # compiled with other tuning macros); by default the in-tree trace build
+    os.environ["LLMOE_LIBRARY"] = os.environ.get("LLMOE_TRACE_LIBRARY") or cuda_build.build(trace=True)
+    import ctypes
+
+    import torch
+
+    from combine_routing_count_prefix_gb300 import llmoe
+    from combine_routing_count_prefix_gb300.inputs import WORKLOADS, make_inputs
+
+    lib = llmoe._lib
+    lib.llmoe_phase_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.llmoe_phase_trace_clear.argtypes = [ctypes.c_void_p]
+    lib.llmoe_trace_empty.argtypes = [ctypes.c_int, ctypes.c_void_p]
+    lib.llmoe_trace_load.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    max_ctas = 8192
+    host = np.zeros((max_ctas, 2 * NPH), dtype=np.uint64)
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    flush_w = torch.empty(FLUSH_BYTES // 8, dtype=torch.int64, device="cuda")
+    flush_r = torch.ones(FLUSH_READ_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def flush():
+        flush_w.zero_()
+        flush_r.sum()
+
+    def traced(launch, steps, mode="flush", warm=None):
+        """Events around `launch`; the stamps of every step.  mode "flush":
+        the bench's L2 flush before each step; "warm-code": the flush, then
+        `warm()` (the same kernel on a tiny separate problem, which brings the
+        kernel's code back into L2 but not this call's data); "no-flush":
+        back-to-back steps."""
+        ev_us, stamps = [], []
+        for i in range(steps + 2):
+            if mode != "no-flush":
+                flush()
+            if mode == "warm-code":
+                warm()
+            llmoe._check(lib.llmoe_phase_trace_clear(sp), "llmoe_phase_trace_clear")
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch()
+            b.record(stream)
+            torch.cuda.synchronize()
+            if i < 2:
+                continue  # warm-up
+            ev_us.append(a.elapsed_time(b) * 1e3)
+            llmoe._check(lib.llmoe_phase_trace_read(host.ctypes.data, max_ctas), "llmoe_phase_trace_read")
+            stamps.append(host[host[:, 0] != 0].astype(np.int64).copy())  # the CTAs that stamped
+        return ev_us, stamps
+
+    def summarize(name, phases, ev_us, stamps):
+        """Means over steps (event times have a coarse tick; the flush between
+        steps puts each step at a random phase of it, so means dither)."""
+        mean = statistics.mean
+        spans, enters, exits = [], [], []
+        per_phase = {p: ([], [], []) for p in range(NPH)}
+        for s in stamps:
+            gt, cy = s[:, :NPH], s[:, NPH:]
+            entry = gt[:, 0]
+            t0 = entry.min()
+            last = np.where(gt[:, NPH - 1] > 0, gt[:, NPH - 1], gt.max(axis=1))
+            spans.append((last.max() - t0) / 1e3)
+            enters.append(((entry - t0).max()) / 1e3)
+            exits.append((np.median(last - t0) / 1e3, (last.max() - t0) / 1e3))
+            for p in range(1, NPH):
+                ok = gt[:, p] > 0
+                if ok.any():
+                    d = (gt[ok, p] - entry[ok]) / 1e3
+                    c = (cy[ok, p] - cy[ok, 0]) / SM_MHZ
+                    per_phase[p][0].append(float(np.median(d)))
+                    per_phase[p][1].append(float(d.max()))
+                    per_phase[p][2].append(float(np.median(c)))
+        ncta = stamps[0].shape[0] if stamps else 0
+        print(f"\n### {name}: {ncta} CTAs, {len(ev_us)} steps")
+        print(f"- CUDA events around the launch: mean {mean(ev_us):.2f} us (min {min(ev_us):.2f})")
+        print(f"- first CTA entry -> last CTA exit: {mean(spans):.2f} us; launch + drain outside it: "
+              f"{mean(ev_us) - mean(spans):.2f} us")
+        print(f"- last CTA entry after the first: {mean(enters):.2f} us; CTA exits after the first entry: "
+              f"median CTA {mean([e[0] for e in exits]):.2f}, last {mean([e[1] for e in exits]):.2f} us")
+        print(f"\n| phase | from CTA entry, median CTA (us) | slowest CTA (us) | median CTA, SM cycles at "
+              f"{SM_MHZ} MHz (us) |")
+        print("|---|---|---|---|")
+        order = sorted((p for p in range(1, NPH) if per_phase[p][0]), key=lambda p: statistics.mean(per_phase[p][0]))
+        for p in order:
+            a, b, c = per_phase[p]
+            if a:
+                print(f"| {phases[p]} | {mean(a):.2f} | {mean(b):.2f} | {mean(c):.2f} |")
+
+    # reference kernels
+    cold = torch.ones(2048 * 4096, dtype=torch.int64, device="cuda")
+    sink = torch.empty(2048, dtype=torch.int64, device="cuda")
+    for ctas in (1, 1024):
+        for mode in ("flush", "no-flush"):
+            ev, st = traced(lambda: llmoe._check(lib.llmoe_trace_empty(ctas, sp), "llmoe_trace_empty"), args.steps,
+                            mode)
+            print(f"\n### empty kernel, {ctas} CTAs, {mode}\n- CUDA events: mean {statistics.mean(ev):.2f} us")
+            ev, st = traced(lambda: llmoe._check(lib.llmoe_trace_load(cold.data_ptr(), sink.data_ptr(), ctas, sp),
+                                                 "llmoe_trace_load"), args.steps, mode)
+            lat = [float(np.median((s[:, 1] - s[:, 0]) / 1e3)) for s in st]
+            print(f"\n### one load per CTA, {ctas} CTAs, {mode}\n- CUDA events: mean {statistics.mean(ev):.2f} us; "
+                  f"load latency (median CTA): {statistics.mean(lat):.2f} us")
+
+    dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    def problem(w):
+        inp = make_inputs(w, seed=0)
+        p = {"x": dev(inp["x"]), "idx": dev(inp["topk_idx"]), "wt": dev(inp["topk_w"]),
+             "y": dev(inp["y_pool"]).index_select(0, dev(inp["y_row_map"])).contiguous(),
+             "out": torch.empty((w.R, w.T, w.H), dtype=torch.int16, device="cuda"),
+             "rb": llmoe.RankBuffers(w.T, w.H, w.R, w.E, fill=0)}
+        F = llmoe.LLMOE_FLAG_CLEAN_OTHER_SET
+        p["bs0"] = p["rb"].buf_set(0, w.K, flags=F)
+        p["bs1"] = p["rb"].buf_set(1, w.K, flags=F | llmoe.LLMOE_FLAG_INPUTS_READY)
+        llmoe.llmoe_clean(p["rb"].buf_set(0, w.K))
+        return p
+
+    tiny = problem(WORKLOADS["tiny"])
+    warm_dispatch = lambda: llmoe.llmoe_dispatch(tiny["x"], tiny["idx"], tiny["bs0"], stream)
+    warm_combine = lambda: llmoe.llmoe_combine(tiny["y"], tiny["idx"], tiny["wt"], tiny["out"], tiny["bs1"], stream)
+    for wname in args.workloads.split(","):
+        w = WORKLOADS[wname]
+        p = problem(w)
+        print(f"\n## {wname}: {w.describe()}")
+        for mode in args.modes.split(","):
+            ev, st = traced(lambda: llmoe.llmoe_dispatch(p["x"], p["idx"], p["bs0"], stream), args.steps, mode,
+                            warm_dispatch)
+            summarize(f"dispatch_kernel, {mode}", PHASES["dispatch"], ev, st)
+            ev, st = traced(lambda: llmoe.llmoe_combine(p["y"], p["idx"], p["wt"], p["out"], p["bs1"], stream),
+                            args.steps, mode, warm_combine)
+            summarize(f"combine_kernel (LLMOE_FLAG_INPUTS_READY), {mode}", PHASES["combine"], ev, st)
+        del p
+        torch.cuda.empty_cache()
+
+
+if __name__ == "__main__":
+    main()
