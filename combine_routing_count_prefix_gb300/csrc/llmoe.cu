@@ -76,31 +76,40 @@ __device__ __forceinline__ void report(int32_t* err, int32_t code) {
 // Phase trace, compiled in only with -DLLMOE_PHASE_TRACE=1 (a separate build
 // of the library; the normal build has none of it).  A traced kernel stamps
 // the global nanosecond timer and its SM's cycle counter at fixed points of
-// its prologue and data phase into a per-CTA row of a device array, which
-// llmoe_phase_trace_read copies out.  Used to find where a kernel's fixed
-// latency goes.
+// its prologue and data phase into a per-CTA row of a device array (the
+// dispatch's CTAs from row 0, the combine's from row kTraceCtas / 2, so one
+// round of both is traced at once), which llmoe_phase_trace_read copies
+// out.  Used to find where a kernel's fixed latency goes.
 #ifndef LLMOE_PHASE_TRACE
 #define LLMOE_PHASE_TRACE 0
 #endif
 #if LLMOE_PHASE_TRACE
-constexpr int kTraceCtas = 8192;
-constexpr int kTracePhases = 8;  // per CTA: kTracePhases timer stamps, kTracePhases cycle stamps
+constexpr int kTraceCtas = 8192;  // rows: dispatch CTAs from 0, combine CTAs from kTraceCtas / 2
+constexpr int kTracePhases = 8;   // per CTA: kTracePhases timer stamps, kTracePhases cycle stamps
 __device__ unsigned long long g_phase_trace[kTraceCtas * 2 * kTracePhases];
-__device__ __forceinline__ void trace_phase(int p) {
-  if (blockIdx.x < kTraceCtas) {
+__device__ __forceinline__ void trace_phase(int base, int p) {
+  const int row = base + (int)blockIdx.x;
+  if (row < kTraceCtas) {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
-    g_phase_trace[(size_t)blockIdx.x * 2 * kTracePhases + p] = t;
-    g_phase_trace[(size_t)blockIdx.x * 2 * kTracePhases + kTracePhases + p] = (unsigned long long)clock64();
+    g_phase_trace[(size_t)row * 2 * kTracePhases + p] = t;
+    g_phase_trace[(size_t)row * 2 * kTracePhases + kTracePhases + p] = (unsigned long long)clock64();
   }
 }
-#define TRACE(p, cond)           \
-  do {                           \
-    if (cond) trace_phase(p);    \
+#define TRACE(p, cond)             \
+  do {                             \
+    if (cond) trace_phase(0, p);   \
+  } while (0)
+#define TRACE_C(p, cond)                          \
+  do {                                            \
+    if (cond) trace_phase(kTraceCtas / 2, p);     \
   } while (0)
 #else
 #define TRACE(p, cond) \
   do {                 \
+  } while (0)
+#define TRACE_C(p, cond) \
+  do {                   \
   } while (0)
 #endif
 
@@ -669,13 +678,13 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
   const int nblock = (t1 - t0) * g.K;
   const float* wblk = topk_w + ((int64_t)src * g.T + t0) * g.K;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  TRACE(0, threadIdx.x == 0);
+  TRACE_C(0, threadIdx.x == 0);
   release_next_grid();
   if (!early) wait_prior_grid();
-  TRACE(1, threadIdx.x == 0);
+  TRACE_C(1, threadIdx.x == 0);
   const float w0 = threadIdx.x < nblock ? wblk[threadIdx.x] : 0.0f;  // before the prologue's barriers
   route_hist(g, idx, src, t0, t1, s, threadIdx.x, blockDim.x);
-  TRACE(2, threadIdx.x == 0);
+  TRACE_C(2, threadIdx.x == 0);
   for (int q = threadIdx.x; q < nblock; q += blockDim.x) {
     const int e = s.ent[q], sl = route_slot(g, s, q);
     const uint4* r = nullptr;
@@ -687,9 +696,9 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
     s_w[q] = q == threadIdx.x ? w0 : wblk[q];
   }
   __syncthreads();
-  TRACE(3, threadIdx.x == 0);
+  TRACE_C(3, threadIdx.x == 0);
   if (early) wait_prior_grid();  // y may come from the previous kernel
-  TRACE(4, threadIdx.x == 0);
+  TRACE_C(4, threadIdx.x == 0);
 
   const int nunits = (t1 - t0) * g.nchunks;
   for (int u = warp; u < nunits; u += kCmbWarps) {
@@ -718,10 +727,10 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
     }
     reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + ((int64_t)src * g.T + t) * g.row_bytes)[j] =
         pack_q<DT>(acc);
-    TRACE(5, threadIdx.x == 0 && u == warp);
+    TRACE_C(5, threadIdx.x == 0 && u == warp);
   }
-  TRACE(6, threadIdx.x == 0);
-  TRACE(7, threadIdx.x == 0);
+  TRACE_C(6, threadIdx.x == 0);
+  TRACE_C(7, threadIdx.x == 0);
 }
 
 // ---------------------------------------------------------------------------

@@ -109,7 +109,8 @@ def main(argv=None):
                 continue  # warm-up
             ev_us.append(a.elapsed_time(b) * 1e3)
             llmoe._check(lib.llmoe_phase_trace_read(host.ctypes.data, max_ctas), "llmoe_phase_trace_read")
-            stamps.append(host[host[:, 0] != 0].astype(np.int64).copy())  # the CTAs that stamped
+            half = host[:max_ctas // 2], host[max_ctas // 2:]  # dispatch rows, combine rows
+            stamps.append(tuple(h[h[:, 0] != 0].astype(np.int64).copy() for h in half))  # the CTAs that stamped
         return ev_us, stamps
 
     def summarize(name, phases, ev_us, stamps):
@@ -150,6 +151,40 @@ def main(argv=None):
             if a:
                 print(f"| {phases[p]} | {mean(a):.2f} | {mean(b):.2f} | {mean(c):.2f} |")
 
+    def timeline(name, ev_us, stamps):
+        """One round on one clock: times relative to the dispatch's first CTA
+        entry, means over steps."""
+        mean = statistics.mean
+        rows = {k: [] for k in ("d_last_entry", "d_exit_med", "d_exit_last", "c_first_entry", "c_entry_med",
+                                "c_wait_min", "c_wait_med", "c_first_unit_med", "c_done_med", "c_exit_last")}
+        for d, c in stamps:
+            t0 = d[:, 0].min()
+            rel = lambda v: (v - t0) / 1e3
+            d_exit = d[:, NPH - 1]
+            rows["d_last_entry"].append(rel(d[:, 0].max()))
+            rows["d_exit_med"].append(rel(np.median(d_exit)))
+            rows["d_exit_last"].append(rel(d_exit.max()))
+            rows["c_first_entry"].append(rel(c[:, 0].min()))
+            rows["c_entry_med"].append(rel(np.median(c[:, 0])))
+            rows["c_wait_min"].append(rel(c[:, 4].min()))
+            rows["c_wait_med"].append(rel(np.median(c[:, 4])))
+            rows["c_first_unit_med"].append(rel(np.median(c[:, 5][c[:, 5] > 0])))
+            rows["c_done_med"].append(rel(np.median(c[:, 6])))
+            rows["c_exit_last"].append(rel(c[:, NPH - 1].max()))
+        r = {k: mean(v) for k, v in rows.items()}
+        print(f"\n### {name}: {len(ev_us)} steps\n- CUDA events around the round: mean {mean(ev_us):.2f} us; "
+              f"first dispatch CTA entry -> last combine CTA exit: {r['c_exit_last']:.2f} us; outside it: "
+              f"{mean(ev_us) - r['c_exit_last']:.2f} us")
+        print("\n| event (from the first dispatch CTA's entry) | us |\n|---|---|")
+        for k, label in (("d_last_entry", "last dispatch CTA entered"), ("d_exit_med", "median dispatch CTA exit"),
+                         ("d_exit_last", "last dispatch CTA exit"), ("c_first_entry", "first combine CTA entered"),
+                         ("c_entry_med", "median combine CTA entered"),
+                         ("c_wait_min", "first combine CTA past its wait for the dispatch"),
+                         ("c_wait_med", "median combine CTA past its wait"),
+                         ("c_first_unit_med", "median combine CTA's first unit stored"),
+                         ("c_done_med", "median combine CTA done"), ("c_exit_last", "last combine CTA exit")):
+            print(f"| {label} | {r[k]:.2f} |")
+
     # reference kernels
     cold = torch.ones(2048 * 4096, dtype=torch.int64, device="cuda")
     sink = torch.empty(2048, dtype=torch.int64, device="cuda")
@@ -160,7 +195,7 @@ def main(argv=None):
             print(f"\n### empty kernel, {ctas} CTAs, {mode}\n- CUDA events: mean {statistics.mean(ev):.2f} us")
             ev, st = traced(lambda: llmoe._check(lib.llmoe_trace_load(cold.data_ptr(), sink.data_ptr(), ctas, sp),
                                                  "llmoe_trace_load"), args.steps, mode)
-            lat = [float(np.median((s[:, 1] - s[:, 0]) / 1e3)) for s in st]
+            lat = [float(np.median((s[0][:, 1] - s[0][:, 0]) / 1e3)) for s in st]
             print(f"\n### one load per CTA, {ctas} CTAs, {mode}\n- CUDA events: mean {statistics.mean(ev):.2f} us; "
                   f"load latency (median CTA): {statistics.mean(lat):.2f} us")
 
@@ -188,10 +223,18 @@ def main(argv=None):
         for mode in args.modes.split(","):
             ev, st = traced(lambda: llmoe.llmoe_dispatch(p["x"], p["idx"], p["bs0"], stream), args.steps, mode,
                             warm_dispatch)
-            summarize(f"dispatch_kernel, {mode}", PHASES["dispatch"], ev, st)
+            summarize(f"dispatch_kernel, {mode}", PHASES["dispatch"], ev, [x[0] for x in st])
             ev, st = traced(lambda: llmoe.llmoe_combine(p["y"], p["idx"], p["wt"], p["out"], p["bs1"], stream),
                             args.steps, mode, warm_combine)
-            summarize(f"combine_kernel (LLMOE_FLAG_INPUTS_READY), {mode}", PHASES["combine"], ev, st)
+            summarize(f"combine_kernel (LLMOE_FLAG_INPUTS_READY), {mode}", PHASES["combine"], ev,
+                      [x[1] for x in st])
+
+            def round_():
+                llmoe.llmoe_dispatch(p["x"], p["idx"], p["bs0"], stream)
+                llmoe.llmoe_combine(p["y"], p["idx"], p["wt"], p["out"], p["bs1"], stream)
+
+            ev, st = traced(round_, args.steps, mode, lambda: (warm_dispatch(), warm_combine()))
+            timeline(f"round (dispatch + combine, as the bench times it), {mode}", ev, st)
         del p
         torch.cuda.empty_cache()
 
