@@ -67,6 +67,10 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-e2e-dense-y", action="store_true", help="skip the e2e leg that uploads the dense y")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-configs", action="store_true", help="skip the other workloads' rounds")
+    p.add_argument("--configs", default="tiny,dsv3,skewed,many_small,large",
+                   help="workloads whose round the line's configs object reports")
+    p.add_argument("--config-steps", type=int, default=50, help="rounds timed per other workload (at most --steps)")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline sample budget")
     return p.parse_args(argv)
 
@@ -464,10 +468,21 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         e2e = run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream)
         e2e["value"] = max_over_ranks([e2e["value"]], world)[0]
 
+    d_us = statistics.mean(disp_ms) * 1e3
+    c_us = statistics.mean(comb_ms) * 1e3
+    configs = None
+    if not args.no_configs:
+        # the other workloads, one at a time on freed memory; this one from the measurements above
+        this = {"round_us": round(round_us, 3), "dispatch_us": round(d_us, 3), "combine_us": round(c_us, 3),
+                "steps": args.steps}
+        del x, idx, wt, y, out, rb, dispatch, combine, dispatch_plain, combine_plain, combine_staged, graph
+        del clean0, clean1, bs0, bs1, bs0_plain, bs1_plain
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        configs = run_configs(args, llmoe, w, this, algo, n_valid, flush, world)
+
     if rank == 0:
         peak, peak_kind = measured_hbm_peak()
-        d_us = statistics.mean(disp_ms) * 1e3
-        c_us = statistics.mean(comb_ms) * 1e3
         dom, dom_us = ("dispatch", d_us) if d_us >= c_us else ("combine", c_us)
         dom_gbs = algo[dom] / dom_us / 1e3
         traffic = ncu_traffic(dom + "_kernel", w.name)
@@ -518,6 +533,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         line["route"] = route
         line["double_buffer"] = pipe
         line["dispatch_unpack"] = signaled
+        if configs is not None:
+            line["configs"] = configs
         if e2e is not None:
             line["e2e"] = e2e
         if not args.no_cpu_baseline:
@@ -526,6 +543,105 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def config_bytes(w, es: int) -> int:
+    """Device bytes one workload needs: the rank buffers, the dense expert
+    outputs y [E*R*T, H], x and the output, with 1 GB to spare."""
+    from combine_routing_count_prefix_gb300 import llmoe
+
+    layout = llmoe.llmoe_layout_bytes_dtype(w.T, w.H, w.R, w.E, llmoe.DTYPE_CODES["fp32" if es == 4 else "bf16"])
+    return w.R * llmoe.round_up(layout, 256) + w.E * w.R * w.T * w.H * es + 2 * w.R * w.T * w.H * es + (1 << 30)
+
+
+def run_configs(args, llmoe, main_w, main_res, main_algo, main_n, flush, world):
+    """Every workload of the bench, measured as the main one is: L2 flushed
+    before each round (outside the events), CUDA events around the two-launch
+    round, then around each kernel.  Returns {workload: figures}; a workload
+    that does not fit in free device memory reports so instead."""
+    import torch
+
+    from combine_routing_count_prefix_gb300.inputs import WORKLOADS, make_inputs
+
+    peak, _ = measured_hbm_peak()
+    es = 4 if args.dtype == "fp32" else 2
+    steps = max(3, min(args.steps, args.config_steps))
+    res = {}
+    for name in args.configs.split(","):
+        w = WORKLOADS[name]
+        r = None
+        if name == main_w.name:
+            r, algo, n_valid = dict(main_res), main_algo, main_n
+        else:
+            free, _total = torch.cuda.mem_get_info()
+            need = config_bytes(w, es)
+            if need <= free:
+                inp = make_inputs(w, seed=args.seed, dtype=args.dtype)
+                n_valid = int((inp["topk_idx"] >= 0).sum())
+                algo = algorithmic_bytes(w, n_valid, w.T, es)
+                r = measure_round(llmoe, w, inp, es, steps, flush)
+                del inp
+                torch.cuda.empty_cache()
+        # every rank takes part in the maximum, measured or not
+        slowest = max_over_ranks([r["round_us"] if r is not None else -1.0], world)[0]
+        if r is None:
+            res[name] = {"shape": w.describe(), "insufficient free HBM":
+                         f"needs {need / 1e9:.1f} GB, {free / 1e9:.1f} GB free"}
+            continue
+        r["round_us"] = slowest
+        gbs = algo["round"] / r["round_us"] / 1e3
+        r.update({"shape": w.describe(), "unmasked_entries": n_valid, "algorithmic_bytes_per_round": algo["round"],
+                  "effective_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+                  "dispatch_frac": round(algo["dispatch"] / r["dispatch_us"] / 1e3 / peak, 4),
+                  "combine_frac": round(algo["combine"] / r["combine_us"] / 1e3 / peak, 4)})
+        res[name] = r
+    return res
+
+
+def measure_round(llmoe, w, inp, es: int, steps: int, flush) -> dict:
+    """The bench round of one workload (dispatch on set 0, combine on set 1,
+    cleans fused) on its own buffers: mean µs of the round, then of each
+    kernel, L2 flushed before every round."""
+    import torch
+
+    dev = lambda a: torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+    x, idx, wt = dev(inp["x"]), dev(inp["topk_idx"]), dev(inp["topk_w"])
+    y = dev(inp["y_pool"]).index_select(0, dev(inp["y_row_map"])).contiguous()
+    out = torch.empty((w.R, w.T, w.H), dtype=torch.float32 if es == 4 else torch.int16, device="cuda")
+    rb = llmoe.RankBuffers(w.T, w.H, w.R, w.E, fill=0, dtype="fp32" if es == 4 else "bf16")
+    F = llmoe.LLMOE_FLAG_CLEAN_OTHER_SET
+    bs0 = rb.buf_set(0, w.K, flags=F)
+    bs1 = rb.buf_set(1, w.K, flags=F | llmoe.LLMOE_FLAG_INPUTS_READY)
+    stream = torch.cuda.current_stream()
+    dispatch = llmoe.bind_dispatch(x, idx, bs0, stream)
+    combine = llmoe.bind_combine(y, idx, wt, out, bs1, stream)
+    llmoe.llmoe_clean(rb.buf_set(0, w.K), stream)
+    for _ in range(3):
+        flush()
+        dispatch()
+        combine()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    ek = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        flush()
+        e[0].record(stream)
+        dispatch()
+        combine()
+        e[1].record(stream)
+    for e in ek:
+        flush()
+        e[0].record(stream)
+        dispatch()
+        e[1].record(stream)
+        combine()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    r = {"round_us": round(statistics.mean(a.elapsed_time(b) for a, b, _ in ev) * 1e3, 3),
+         "dispatch_us": round(statistics.mean(a.elapsed_time(b) for a, b, _ in ek) * 1e3, 3),
+         "combine_us": round(statistics.mean(b.elapsed_time(c) for _, b, c in ek) * 1e3, 3), "steps": steps}
+    del dispatch, combine, x, idx, wt, y, out, rb
+    return r
 
 
 def run_route(llmoe, w, idx, rb, tokens, flush, steps: int = 200):

@@ -15,7 +15,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 @pytest.mark.gpu
 def test_bench_line_on_tiny():
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "tiny", "--steps", "20",
-                          "--warmup", "3", "--e2e-steps", "5", "--cpu-seconds", "1"],
+                          "--warmup", "3", "--e2e-steps", "5", "--cpu-seconds", "1", "--configs", "tiny,many_small",
+                          "--config-steps", "5"],
                          capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert res.returncode == 0, res.stderr[-3000:]
     lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
@@ -36,3 +37,9 @@ def test_bench_line_on_tiny():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    cf = d["configs"]  # every requested workload's round, measured the same way
+    assert set(cf) == {"tiny", "many_small"}
+    for name, c in cf.items():
+        for key in ("round_us", "dispatch_us", "combine_us", "effective_gbs", "frac_of_measured_hbm", "shape"):
+            assert key in c, (name, key)
+        assert c["round_us"] > 0 and c["dispatch_us"] > 0 and c["combine_us"] > 0
