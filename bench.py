@@ -831,12 +831,20 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
         return statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3, n
 
     us, n = timed(layer)
-    res = {"value": round(us, 2), "unit": "us/round", "h2d_bytes_per_step": hin.numel(),
-           "d2h_bytes_per_step": d2h, "steps": n, "launches_per_step": 3,
-           "note": "one MoE layer with identity experts through the C ABI: x, topk_idx, topk_w copied "
-                   "host->device in one copy from one pinned buffer; llmoe_dispatch; llmoe_unpack (the experts' "
-                   "input rows, which identity experts return as their output y); llmoe_combine over them; the "
-                   "output copied back"}
+    serial = {"value": round(us, 2), "unit": "us/round", "steps": n,
+              "note": "the same layer with each step's copies and kernels one after another on one stream"}
+    pipe = run_e2e_pipelined(args, llmoe, w, hin, hout, rb, tokens, stream)
+    ceil = copy_ceiling(hin, hout)
+    res = {"value": pipe["value"], "unit": "us/round", "h2d_bytes_per_step": hin.numel(),
+           "d2h_bytes_per_step": d2h, "steps": pipe["steps"], "launches_per_step": 3,
+           "note": "one MoE layer with identity experts through the C ABI, steps back to back: x, topk_idx, topk_w "
+                   "copied host->device in one copy from one pinned buffer; llmoe_dispatch; llmoe_unpack (the "
+                   "experts' input rows, which identity experts return as their output y); llmoe_combine over "
+                   "them; the output copied back.  Uploads and downloads run on their own streams into double "
+                   "buffers, so step i+1's upload and step i-1's download overlap step i's kernels; value = time "
+                   "from the first upload to the last download / steps",
+           "serial": serial, "copy_ceiling": ceil,
+           "copy_gbs": round((hin.numel() + d2h) / (pipe["copy_us_per_step"] * 1e3), 1)}
     del recv_x, recv_src
     if not args.no_e2e_dense_y:
         hy = torch.from_numpy(dense_y(inp).view(np.int16) if pay == torch.int16 else dense_y(inp)).pin_memory()
@@ -856,6 +864,102 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
                           "note": "the bench round with the dense expert outputs y [E*R*T, H] also copied "
                                   "host->device every step"}
     return res
+
+
+def copy_ceiling(hin, hout, reps: int = 20) -> dict:
+    """Pinned host <-> device copy rates of the e2e step's sizes, each copy
+    alone on the current stream (CUDA events, mean of `reps`)."""
+    import torch
+
+    din = torch.empty_like(hin, device="cuda")
+    dout = torch.empty_like(hout, device="cuda")
+    cur = torch.cuda.current_stream()
+    res = {}
+    for name, dst, src in (("h2d", din, hin), ("d2h", hout, dout)):
+        dst.copy_(src, non_blocking=True)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in evs:
+            a.record(cur)
+            dst.copy_(src, non_blocking=True)
+            b.record(cur)
+        torch.cuda.synchronize()
+        us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+        nbytes = src.numel() * src.element_size()
+        res[name] = {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1), "bytes": nbytes}
+    return res
+
+
+def run_e2e_pipelined(args, llmoe, w, hin, hout, rb, tokens, stream):
+    """The e2e layer, steps back to back with their copies overlapped: step
+    i's upload (its own stream, into input buffer i % 2) waits only for the
+    kernels of step i-2 that read that buffer; step i's kernels wait for its
+    upload and for the download of step i-2 from output buffer i % 2; step
+    i's download (its own stream) waits for its kernels.  The kernels stay on
+    one stream in order (consecutive steps share the rank buffers)."""
+    import torch
+
+    x_b = w.R * tokens * w.H * (hout.element_size())
+    idx_b = w.R * tokens * w.K * 8
+    pay = hout.dtype
+    din = [torch.empty_like(hin, device="cuda") for _ in (0, 1)]
+    dout = [torch.empty((w.R, tokens, w.H), dtype=pay, device="cuda") for _ in (0, 1)]
+    rows = w.E * w.R * w.T
+    recv_x = torch.empty((rows, w.H), dtype=pay, device="cuda")
+    recv_src = torch.empty((rows,), dtype=torch.int32, device="cuda")
+    F = llmoe.LLMOE_FLAG_CLEAN_OTHER_SET
+    bs0 = rb.buf_set(0, w.K, flags=F)
+    bs1 = rb.buf_set(1, w.K, flags=F | llmoe.LLMOE_FLAG_INPUTS_READY)
+    views = []
+    for d in din:
+        views.append((d[:x_b].view(pay).view(w.R, tokens, w.H), d[x_b:x_b + idx_b].view(torch.int64).view(w.R, tokens, w.K),
+                      d[x_b + idx_b:].view(torch.float32).view(w.R, tokens, w.K)))
+    s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+    up_done = [torch.cuda.Event() for _ in (0, 1)]
+    comp_done = [torch.cuda.Event() for _ in (0, 1)]
+    down_done = [torch.cuda.Event() for _ in (0, 1)]
+
+    def run(n):
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_up):
+                if i >= 2:
+                    s_up.wait_event(comp_done[b])
+                din[b].copy_(hin, non_blocking=True)
+                up_done[b].record(s_up)
+            stream.wait_event(up_done[b])
+            if i >= 2:
+                stream.wait_event(down_done[b])
+            dx, didx, dw = views[b]
+            llmoe.llmoe_dispatch(dx, didx, bs0, stream)
+            llmoe.llmoe_unpack(recv_x, recv_src, bs0, stream)
+            llmoe.llmoe_combine(recv_x, didx, dw, dout[b], bs1, stream)
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(comp_done[b])
+                hout.copy_(dout[b], non_blocking=True)
+                down_done[b].record(s_down)
+
+    llmoe.llmoe_clean(rb.buf_set(0, w.K), stream)
+    run(4)
+    torch.cuda.synchronize()
+    n = max(4, args.e2e_steps)
+    a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_up)
+    stream.wait_event(a)
+    run(n)
+    s_down.wait_event(comp_done[(n - 1) % 2])
+    b_.record(s_down)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b_) * 1e3 / n
+    # the copies alone, as this schedule issues them (for the overlap achieved)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for i in range(n):
+        din[i % 2].copy_(hin, non_blocking=True)
+        hout.copy_(dout[i % 2], non_blocking=True)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    return {"value": round(us, 2), "steps": n, "copy_us_per_step": c0.elapsed_time(c1) * 1e3 / n}
 
 
 def main(argv=None):

@@ -873,6 +873,10 @@ __device__ __forceinline__ uint4 ld_payload_quad(const uint8_t* pay, int phase, 
 #endif
 constexpr int kReduceBatch = LLMOE_REDUCE_KBATCH;  // messages whose loads a warp has in flight at once
 
+// Each warp takes a contiguous range of the R * T * nchunks (token, chunk)
+// units, so it meets a new token once per nchunks units at most: lanes k < K
+// then load that token's expert id and weight (one memory round trip), and
+// every unit of the token reuses them from registers.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) combine_reduce_kernel(Geometry g, const int64_t* __restrict__ idx,
                                                                      const float* __restrict__ topk_w,
@@ -882,15 +886,24 @@ __global__ void __launch_bounds__(kThreads, 4) combine_reduce_kernel(Geometry g,
   const int lane = threadIdx.x & 31;
   const int64_t nunits = (int64_t)g.R * g.T * g.nchunks;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t u = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; u < nunits; u += nwarps) {
-    const int64_t tok = u / g.nchunks;
-    const int c = (int)(u - tok * g.nchunks);
-    const int src = (int)(tok / g.T), t = (int)(tok - (int64_t)src * g.T);
-    long long e_lane = -1;
-    float w_lane = 0.0f;
-    if (lane < g.K) {
-      e_lane = idx[tok * g.K + lane];
-      w_lane = topk_w[tok * g.K + lane];
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t ubeg = nunits * gw / nwarps, uend = nunits * (gw + 1) / nwarps;
+  if (ubeg >= uend) return;
+  int64_t tok = ubeg / g.nchunks;  // walked forward unit by unit from here
+  int c = (int)(ubeg - tok * g.nchunks);
+  int src = (int)(tok / g.T), t = (int)(tok - (int64_t)src * g.T);
+  bool fresh = true;
+  long long e_lane = -1;
+  float w_lane = 0.0f;
+  for (int64_t left = uend - ubeg; left > 0; --left) {
+    if (fresh) {  // the whole warp: lane k holds entry k of the token
+      e_lane = -1;
+      w_lane = 0.0f;
+      if (lane < g.K) {
+        e_lane = idx[tok * g.K + lane];
+        w_lane = topk_w[tok * g.K + lane];
+      }
+      fresh = false;
     }
     const int j = c * 32 + lane;
     const uint8_t* rbase = g.base + src * g.rank_stride + g.recv_off;
@@ -927,6 +940,15 @@ __global__ void __launch_bounds__(kThreads, 4) combine_reduce_kernel(Geometry g,
     if (j < g.nq)
       reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + ((int64_t)src * g.T + t) * g.row_bytes)[j] =
           pack_q<DT>(acc);
+    if (++c == g.nchunks) {  // the next token
+      c = 0;
+      ++tok;
+      if (++t == g.T) {
+        t = 0;
+        ++src;
+      }
+      fresh = true;
+    }
   }
 }
 
@@ -1622,7 +1644,10 @@ constexpr int kStaticMaxRanks = LLMOE_STATIC_MAX_RANKS;
 static __device__ __align__(256) int32_t g_static_counters[kStaticMaxRanks + 1];  // per source, plus the consumers'
 
 // The array's device address, looked up once per device (with that device
-// current): host code must not hand the symbol itself to a kernel.
+// current): host code must not hand the symbol itself to a kernel.  The
+// address is kept for the life of the process; after a cudaDeviceReset the
+// module may be loaded again elsewhere, so the library must not be called on
+// a device after it has been reset.
 std::atomic<int32_t*> g_static_counters_addr[kMaxDevices];
 
 int static_counters(int32_t** out) {
@@ -1692,6 +1717,60 @@ __global__ void trace_load_kernel(const int64_t* p, int64_t* out) {
   }
 }
 #endif
+
+// A checked signalled-dispatch launch: geometry, grid and shared memory.
+struct SignaledLaunch {
+  Geometry g;
+  int64_t grid;
+  size_t smem;
+};
+
+// Every argument and residency check of llmoe_dispatch_signaled (and of its
+// static variant) except the workspace pointer; nothing is queued.
+int prepare_signaled(const void* x, const int64_t* topk_idx, const void* recv_x, const int32_t* recv_src,
+                     int64_t spin_limit, const llmoe_buf_set_t* bs, SignaledLaunch* out) {
+  Geometry& g = out->g;
+  int rc = make_geometry(bs, true, &g);
+  if (rc != LLMOE_SUCCESS) return rc;
+  if ((g.T > 0 && (x == nullptr || topk_idx == nullptr || !aligned(x, 16) || !aligned(topk_idx, 8))) ||
+      recv_x == nullptr || recv_src == nullptr || !aligned(recv_x, 16) || !aligned(recv_src, 4) || spin_limit < 1)
+    return LLMOE_ERR_INVALID_ARGUMENT;
+  const size_t smem_one = route_smem_bytes(g) + sizeof(uintptr_t) * (size_t)g.K;
+  const int occ = blocks_per_sm(kslot(kSignaledKernel), (const void*)dispatch_signaled_kernel, kThreads, smem_one);
+  set_blocking(&g, occ);
+  out->smem = route_smem_bytes(g) + sizeof(uintptr_t) * (size_t)g.TB * g.K;
+  if ((rc = set_smem(kslot(kSignaledKernel), (const void*)dispatch_signaled_kernel, out->smem)) != LLMOE_SUCCESS)
+    return rc;
+  int fit = 0;  // the exact smem of this launch may lower the occupancy
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, (const void*)dispatch_signaled_kernel, kThreads,
+                                                    out->smem) != cudaSuccess) {
+    cudaGetLastError();
+    return LLMOE_ERR_CUDA;
+  }
+  out->grid = (int64_t)g.R * g.nblk;
+  if (out->grid > (int64_t)num_sms() * fit) return LLMOE_ERR_INVALID_ARGUMENT;  // not all CTAs could be resident
+  return LLMOE_SUCCESS;
+}
+
+int launch_signaled(const SignaledLaunch& sl, const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src,
+                    int32_t* counters, int64_t spin_limit, llmoe_stream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sl.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sl.smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, dispatch_signaled_kernel, sl.g, x, topk_idx, recv_x, recv_src, counters,
+                         (long long)spin_limit) != cudaSuccess) {
+    cudaGetLastError();
+    return LLMOE_ERR_CUDA;
+  }
+  return LLMOE_SUCCESS;
+}
 
 }  // namespace
 
@@ -1832,60 +1911,32 @@ size_t llmoe_signal_workspace_bytes(const llmoe_buf_set_t* bs) {
 
 int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src, void* workspace,
                             int64_t spin_limit, const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
-  Geometry g;
-  int rc = make_geometry(bs, true, &g);
+  SignaledLaunch sl;
+  const int rc = prepare_signaled(x, topk_idx, recv_x, recv_src, spin_limit, bs, &sl);
   if (rc != LLMOE_SUCCESS) return rc;
-  if ((g.T > 0 && (x == nullptr || topk_idx == nullptr || !aligned(x, 16) || !aligned(topk_idx, 8))) ||
-      recv_x == nullptr || recv_src == nullptr || !aligned(recv_x, 16) || !aligned(recv_src, 4) ||
-      workspace == nullptr || !aligned(workspace, 4) || spin_limit < 1)
-    return LLMOE_ERR_INVALID_ARGUMENT;
-  const size_t smem_one = route_smem_bytes(g) + sizeof(uintptr_t) * (size_t)g.K;
-  const int occ = blocks_per_sm(kslot(kSignaledKernel), (const void*)dispatch_signaled_kernel, kThreads, smem_one);
-  set_blocking(&g, occ);
-  const size_t smem = route_smem_bytes(g) + sizeof(uintptr_t) * (size_t)g.TB * g.K;
-  if ((rc = set_smem(kslot(kSignaledKernel), (const void*)dispatch_signaled_kernel, smem)) != LLMOE_SUCCESS)
-    return rc;
-  int fit = 0;  // the exact smem of this launch may lower the occupancy
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, (const void*)dispatch_signaled_kernel, kThreads, smem) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    return LLMOE_ERR_CUDA;
-  }
-  const int64_t grid = (int64_t)g.R * g.nblk;
-  if (grid > (int64_t)num_sms() * fit) return LLMOE_ERR_INVALID_ARGUMENT;  // not all CTAs could be resident
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = (cudaStream_t)stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, dispatch_signaled_kernel, g, x, topk_idx, recv_x, recv_src,
-                         static_cast<int32_t*>(workspace), (long long)spin_limit) != cudaSuccess) {
-    cudaGetLastError();
-    return LLMOE_ERR_CUDA;
-  }
-  return LLMOE_SUCCESS;
+  if (workspace == nullptr || !aligned(workspace, 4)) return LLMOE_ERR_INVALID_ARGUMENT;
+  return launch_signaled(sl, x, topk_idx, recv_x, recv_src, static_cast<int32_t*>(workspace), spin_limit, stream);
 }
 
 int llmoe_dispatch_signaled_static(const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src,
                                    int64_t spin_limit, const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
   if (bs == nullptr || bs->num_ranks < 1) return LLMOE_ERR_INVALID_ARGUMENT;
   if (bs->num_ranks > kStaticMaxRanks) return LLMOE_ERR_INVALID_ARGUMENT;  // more ranks than the array holds
-  int32_t* counters = nullptr;
-  int rc = static_counters(&counters);
+  // every check before anything is queued: a rejected call leaves the
+  // shared counters alone
+  SignaledLaunch sl;
+  int rc = prepare_signaled(x, topk_idx, recv_x, recv_src, spin_limit, bs, &sl);
   if (rc != LLMOE_SUCCESS) return rc;
-  // the counters must start at zero; a previous call may have left them
-  // otherwise (a timeout), so clear the part this call uses, in stream order
+  int32_t* counters = nullptr;
+  if ((rc = static_counters(&counters)) != LLMOE_SUCCESS) return rc;
+  // the counters must start at zero; clear the part this call uses, in
+  // stream order
   if (cudaMemsetAsync(counters, 0, sizeof(int32_t) * (size_t)(bs->num_ranks + 1), (cudaStream_t)stream) !=
       cudaSuccess) {
     cudaGetLastError();
     return LLMOE_ERR_CUDA;
   }
-  return llmoe_dispatch_signaled(x, topk_idx, recv_x, recv_src, counters, spin_limit, bs, stream);
+  return launch_signaled(sl, x, topk_idx, recv_x, recv_src, counters, spin_limit, stream);
 }
 
 int llmoe_clean(const llmoe_buf_set_t* bs, llmoe_stream_t stream) {

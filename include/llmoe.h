@@ -285,10 +285,15 @@ LLMOE_API int llmoe_dispatch_signaled(const void* x, const int64_t* topk_idx, vo
  *     workspace.  num_ranks above LLMOE_STATIC_MAX_RANKS returns
  *     LLMOE_ERR_INVALID_ARGUMENT without launching.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and keeps it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and keeps it for the
+ *     life of the process; make that first call before any stream capture,
+ *     and make no call on a device after a cudaDeviceReset of it (the
+ *     array may then sit at another address).
+ *   - Every argument check comes first: a call that returns an error has
+ *     queued nothing and left the array alone.
  *   - Each call clears the counters it uses (a cudaMemsetAsync on `stream`)
- *     before its kernel, so a timed-out earlier call leaves no residue.
+ *     before its kernel.  A launch returns them to zero itself, timed out
+ *     or not; the clear covers a launch that never finished.
  *   - All calls on a device share the one array: calls whose kernels
  *     overlap on the GPU (on different streams) race on it and must not be
  *     issued that way. */

@@ -6,12 +6,14 @@ loop that must not cudaMalloc) use this variant: its workspace is a fixed
 array inside the library.  This file sorts last so that a run stopping at the
 first failure has run every other test; it also passes on its own.  Its
 results must equal those of llmoe_dispatch_signaled with a caller-allocated
-workspace, bit for bit, on two calls in a row.
+workspace, bit for bit, on two calls in a row, and the CPU oracle's
+messages, counts and unpacked rows.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from combine_routing_count_prefix_gb300.inputs import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -25,6 +27,7 @@ def L():
     from combine_routing_count_prefix_gb300 import llmoe
 
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    oracle.build()
     return llmoe
 
 
@@ -62,9 +65,46 @@ def test_static_workspace_matches_caller_workspace(L, name):
         assert torch.equal(rs_a, rs_b), f"call {call}: source tokens differ"
         assert torch.equal(rb_a.storage, rb_b.storage), f"call {call}: rank buffers differ"
         assert (rs_b >= 0).sum().item() == int((inp["topk_idx"] >= 0).sum())
+        check_against_oracle(rb_b, rx_b, rs_b, inp, w)
+
+
+def check_against_oracle(rb, recv_x, recv_src, inp, w):
+    """Messages, count words and unpacked rows equal the CPU oracle's."""
+    d = oracle.dispatch(inp["x"], inp["topk_idx"], w.E, num_max_tokens=w.T)
+    got = rb.recv_rows(0)[dev(d["row_rank"]), dev(d["row_index"])].cpu().numpy()
+    assert np.array_equal(got, d["msgs"]), "dispatch messages differ from the oracle"
+    assert np.array_equal(rb.signal_words(0).cpu().numpy(), d["count_words"]), "count words differ"
+    u = oracle.unpack(inp["x"], inp["topk_idx"], w.E, num_max_tokens=w.T)
+    rows = u["rows"]
+    gx, gs = recv_x.cpu().numpy(), recv_src.cpu().numpy()
+    assert np.array_equal(gx[rows].view(np.uint16), u["recv_x"][rows]), "unpacked rows differ from the oracle"
+    assert np.array_equal(gs[rows], u["recv_src"][rows]), "unpacked source tokens differ from the oracle"
+
+
+@pytest.mark.parametrize("name", ["skewed", "dsv3"])
+def test_static_workspace_matches_oracle_after_a_timed_out_call(L, name):
+    """A call whose consumers give up at once (a one-cycle spin limit, so most
+    of them time out), then a normal call: the second call's results are the
+    oracle's, whatever the first left behind."""
+    w = WORKLOADS[name]
+    rb, bs, recv_x, recv_src, err = outputs(L, w)
+    inp = make_inputs(w, seed=93)
+    x, idx = dev(inp["x"]), dev(inp["topk_idx"])
+    L.llmoe_clean(bs)
+    L.llmoe_dispatch_signaled_static(x, idx, recv_x, recv_src, 1, bs)
+    torch.cuda.synchronize()
+    assert L.llmoe_get_error(bs, reset=True) in (L.LLMOE_DEV_OK, L.LLMOE_DEV_TIMEOUT)
+    recv_src.fill_(-7)
+    L.llmoe_clean(bs)
+    L.llmoe_dispatch_signaled_static(x, idx, recv_x, recv_src, 2_000_000_000, bs)
+    torch.cuda.synchronize()
+    assert L.llmoe_get_error(bs) == 0
+    check_against_oracle(rb, recv_x, recv_src, inp, w)
 
 
 def test_static_workspace_rejects_too_many_ranks(L):
+    # rejected on the host before anything is queued (the pointers are never
+    # dereferenced)
     w = WORKLOADS["tiny"].with_(R=L.LLMOE_STATIC_MAX_RANKS + 1, E=L.LLMOE_STATIC_MAX_RANKS + 1, K=1, T=1, H=8)
     bs = L.llmoe_buf_set_t(base=1 << 20, rank_stride=1 << 20, num_max_tokens=w.T, num_tokens=w.T, hidden=w.H,
                            num_ranks=w.R, num_experts=w.E, num_topk=w.K, set=0, err=None, flags=0, dtype=0)
