@@ -67,6 +67,8 @@ struct Geometry {
   int nchunks;  // warp units per row, ceil(nq / 32)
   int TB;       // tokens per CTA
   int nblk;     // token blocks per source rank
+  int dsplit;   // dispatch: data CTAs per token block (each a share of the rows' ring chunks)
+  int csplit;   // combine: data CTAs per token block (each a share of the rows' 512 B chunks)
 };
 
 __device__ __forceinline__ void report(int32_t* err, int32_t code) {
@@ -84,16 +86,23 @@ __device__ __forceinline__ void report(int32_t* err, int32_t code) {
 #define LLMOE_PHASE_TRACE 0
 #endif
 #if LLMOE_PHASE_TRACE
-constexpr int kTraceCtas = 8192;  // rows: dispatch CTAs from 0, combine CTAs from kTraceCtas / 2
+constexpr int kTraceCtas = 65536;  // rows: dispatch CTAs from 0, combine CTAs from kTraceCtas / 2
 constexpr int kTracePhases = 8;   // per CTA: kTracePhases timer stamps, kTracePhases cycle stamps
 __device__ unsigned long long g_phase_trace[kTraceCtas * 2 * kTracePhases];
+// The cycle slot of phase 0 holds the CTA's SM id instead.
 __device__ __forceinline__ void trace_phase(int base, int p) {
   const int row = base + (int)blockIdx.x;
   if (row < kTraceCtas) {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
     g_phase_trace[(size_t)row * 2 * kTracePhases + p] = t;
-    g_phase_trace[(size_t)row * 2 * kTracePhases + kTracePhases + p] = (unsigned long long)clock64();
+    unsigned long long c = (unsigned long long)clock64();
+    if (p == 0) {
+      unsigned smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      c = smid;
+    }
+    g_phase_trace[(size_t)row * 2 * kTracePhases + kTracePhases + p] = c;
   }
 }
 #define TRACE(p, cond)             \
@@ -423,6 +432,21 @@ constexpr int kDspChunk = kDspConsumers * 32 * 16;   // x bytes per stage
 constexpr int kDspStageBytes = kDspChunk + 16;       // + the quad before the chunk
 constexpr int kDspStages = LLMOE_DSP_STAGES;
 constexpr int kDspThreads = 32 * (1 + kDspConsumers);
+// A grid with several tokens per CTA (TB > 1: more tokens than one wave of
+// CTAs, e.g. 8 ranks x 1,024 tokens) is split further: each token block gets
+// up to LLMOE_DSP_SPLIT dispatch CTAs (one per 2 KB ring chunk of its rows) and
+// LLMOE_CMB_SPLIT combine CTAs, each moving a contiguous share of the rows'
+// chunks.  The grid then spans many waves and the CTA scheduler gives the SMs
+// that move rows fastest more CTAs: a GB300's SMs do not move rows at one rate
+// (per-SM rates measured in the dispatch differ by up to 1.9x, in groups of
+// SMs), and with one wave of equal CTAs the slowest group sets the kernel's
+// end.  With one token per CTA the split only repeats the route scan.
+#ifndef LLMOE_DSP_SPLIT
+#define LLMOE_DSP_SPLIT 64
+#endif
+#ifndef LLMOE_CMB_SPLIT
+#define LLMOE_CMB_SPLIT 2
+#endif
 #ifndef LLMOE_DSP_DEST_REGS
 #define LLMOE_DSP_DEST_REGS 8
 #endif
@@ -458,11 +482,14 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
   }
 
   const int bid = (int)blockIdx.x - g.R;
-  const int src = bid / g.nblk, b = bid % g.nblk;
+  const int part = bid % g.dsplit;
+  const int src = bid / g.dsplit / g.nblk, b = bid / g.dsplit % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row_bytes = g.row_bytes;
-  const int nch = (row_bytes + kDspChunk - 1) / kDspChunk;
+  const int nch_row = (row_bytes + kDspChunk - 1) / kDspChunk;
+  const int c0 = nch_row * part / g.dsplit;  // this CTA's chunks [c0, c0 + nch) of each of its rows
+  const int nch = nch_row * (part + 1) / g.dsplit - c0;
   const int n_iters = (t1 - t0) * nch;
   TRACE(0, threadIdx.x == 0);
 
@@ -488,7 +515,7 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
       for (; next < n_iters; ++next) {
         const int sidx = next % kDspStages, use = next / kDspStages;
         if (use > 0 && !mbar_wait(&ring.empty[sidx], (use - 1) & 1, g.err)) break;
-        const int tl = next / nch, c = next % nch;
+        const int tl = next / nch, c = c0 + next % nch;
         const int len = min(kDspChunk, row_bytes - c * kDspChunk);
         uint8_t* dst = ring.stage(sidx);
         const uint8_t* row = xsrc + (size_t)tl * row_bytes;
@@ -530,7 +557,7 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
       const int sidx = it % kDspStages;
       if (!mbar_wait(&ring.full[sidx], (it / kDspStages) & 1, g.err)) break;
       TRACE(5, threadIdx.x == 32 && it == 0);
-      const int tl = it / nch, c = it % nch;
+      const int tl = it / nch, c = c0 + it % nch;
       const int len = min(kDspChunk, row_bytes - c * kDspChunk);
       const uint8_t* sb = ring.stage(sidx);
       const uintptr_t* dsts = s_dst + tl * g.K;
@@ -673,7 +700,8 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
   }
 
   const int bid = (int)blockIdx.x - g.R;
-  const int src = bid / g.nblk, b = bid % g.nblk;
+  const int part = bid % g.csplit;
+  const int src = bid / g.csplit / g.nblk, b = bid / g.csplit % g.nblk;
   const int t0 = b * g.TB, t1 = min(g.T, t0 + g.TB);
   const int nblock = (t1 - t0) * g.K;
   const float* wblk = topk_w + ((int64_t)src * g.T + t0) * g.K;
@@ -700,9 +728,10 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
   if (early) wait_prior_grid();  // y may come from the previous kernel
   TRACE_C(4, threadIdx.x == 0);
 
-  const int nunits = (t1 - t0) * g.nchunks;
+  const int c0 = g.nchunks * part / g.csplit, cn = g.nchunks * (part + 1) / g.csplit - c0;  // this CTA's chunks
+  const int nunits = (t1 - t0) * cn;
   for (int u = warp; u < nunits; u += kCmbWarps) {
-    const int tl = u / g.nchunks, c = u % g.nchunks;
+    const int tl = u / cn, c = c0 + u % cn;
     const int t = t0 + tl;
     const int j = c * 32 + lane;
     if (j >= g.nq) continue;
@@ -1522,6 +1551,8 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   g->nchunks = (g->nq + 31) / 32;
   g->TB = 1;
   g->nblk = T > 0 ? T : 1;
+  g->dsplit = 1;
+  g->csplit = 1;
   return LLMOE_SUCCESS;
 }
 
@@ -1675,13 +1706,16 @@ int static_counters(int32_t** out) {
 
 // Dispatch and combine grids: R count CTAs, then R * nblk data CTAs (none
 // when the call has no tokens).
-unsigned count_and_data_ctas(const Geometry& g) { return (unsigned)(g.R + (g.T > 0 ? g.R * g.nblk : 0)); }
+unsigned count_and_data_ctas(const Geometry& g) {
+  return (unsigned)(g.R + (g.T > 0 ? g.R * g.nblk * g.dsplit * g.csplit : 0));
+}
 
 template <int DT>
 int launch_combine(Geometry& g, const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                    llmoe_stream_t stream) {
   const int id = kslot(kCombineKernel, DT);
   set_blocking(&g, blocks_per_sm(id, (const void*)combine_kernel<DT>, kCmbThreads, combine_smem_bytes(g)), g.R);
+  g.csplit = g.TB > 1 ? std::max(1, std::min(LLMOE_CMB_SPLIT, g.nchunks)) : 1;
   const size_t smem = combine_smem_bytes(g);
   const int rc = set_smem(id, (const void*)combine_kernel<DT>, smem);
   if (rc != LLMOE_SUCCESS) return rc;
@@ -1826,6 +1860,8 @@ int llmoe_dispatch(const void* x, const int64_t* topk_idx, const llmoe_buf_set_t
     return LLMOE_ERR_INVALID_ARGUMENT;
   set_blocking(&g, blocks_per_sm(kslot(kDispatchKernel), (const void*)dispatch_kernel, kDspThreads, dispatch_smem_bytes(g)),
                g.R);
+  const int nch_row = (g.row_bytes + kDspChunk - 1) / kDspChunk;
+  g.dsplit = g.TB > 1 ? std::max(1, std::min(LLMOE_DSP_SPLIT, nch_row)) : 1;
   const size_t smem = dispatch_smem_bytes(g);
   if ((rc = set_smem(kslot(kDispatchKernel), (const void*)dispatch_kernel, smem)) != LLMOE_SUCCESS) return rc;
   return launch(dispatch_kernel, count_and_data_ctas(g), kDspThreads, smem, stream, g, x, topk_idx);

@@ -55,6 +55,7 @@ def main(argv=None):
     ap.add_argument("--workloads", default="tiny,many_small,skewed,dsv3")
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--modes", default="flush,warm-code,no-flush")
+    ap.add_argument("--dump", default="", help="directory for every CTA's stamps (an .npz per workload and mode)")
     args = ap.parse_args(argv)
 
     from combine_routing_count_prefix_gb300 import build as cuda_build
@@ -74,7 +75,7 @@ def main(argv=None):
     lib.llmoe_phase_trace_clear.argtypes = [ctypes.c_void_p]
     lib.llmoe_trace_empty.argtypes = [ctypes.c_int, ctypes.c_void_p]
     lib.llmoe_trace_load.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
-    max_ctas = 8192
+    max_ctas = 65536  # trace rows: the dispatch's CTAs, then the combine's from max_ctas / 2
     host = np.zeros((max_ctas, 2 * NPH), dtype=np.uint64)
 
     torch.cuda.set_device(0)
@@ -131,7 +132,7 @@ def main(argv=None):
                 ok = gt[:, p] > 0
                 if ok.any():
                     d = (gt[ok, p] - entry[ok]) / 1e3
-                    c = (cy[ok, p] - cy[ok, 0]) / SM_MHZ
+                    c = (cy[ok, p] - cy[ok, 1]) / SM_MHZ + (gt[ok, 1] - gt[ok, 0]) / 1e3  # slot 0 holds the SM id
                     per_phase[p][0].append(float(np.median(d)))
                     per_phase[p][1].append(float(d.max()))
                     per_phase[p][2].append(float(np.median(c)))
@@ -143,7 +144,7 @@ def main(argv=None):
         print(f"- last CTA entry after the first: {mean(enters):.2f} us; CTA exits after the first entry: "
               f"median CTA {mean([e[0] for e in exits]):.2f}, last {mean([e[1] for e in exits]):.2f} us")
         print(f"\n| phase | from CTA entry, median CTA (us) | slowest CTA (us) | median CTA, SM cycles at "
-              f"{SM_MHZ} MHz (us) |")
+              f"{SM_MHZ} MHz from phase 1, plus phase 1 (us) |")
         print("|---|---|---|---|")
         order = sorted((p for p in range(1, NPH) if per_phase[p][0]), key=lambda p: statistics.mean(per_phase[p][0]))
         for p in order:
@@ -235,6 +236,12 @@ def main(argv=None):
 
             ev, st = traced(round_, args.steps, mode, lambda: (warm_dispatch(), warm_combine()))
             timeline(f"round (dispatch + combine, as the bench times it), {mode}", ev, st)
+            if args.dump:
+                os.makedirs(args.dump, exist_ok=True)
+                # per step: [CTA, 2 * NPH] stamps (globaltimer phases, then SM cycles; cycle slot 0 = SM id)
+                np.savez_compressed(os.path.join(args.dump, f"round_{wname}_{mode}.npz"),
+                                    **{f"dispatch_{i}": d for i, (d, _) in enumerate(st)},
+                                    **{f"combine_{i}": c for i, (_, c) in enumerate(st)})
         del p
         torch.cuda.empty_cache()
 

@@ -226,6 +226,17 @@ def test_long_prefix_many_tokens_per_cta(L):
     full_check(Round(L, w, seed=6))
 
 
+@pytest.mark.parametrize("dtype,tokens", [("bf16", None), ("fp32", None), ("bf16", 599)])
+def test_split_grids_several_tokens_per_cta(L, dtype, tokens):
+    # more tokens than one wave of CTAs (several tokens per CTA), so the
+    # dispatch gives each token block one CTA per ring chunk of its rows and
+    # the combine two CTAs per block; rows of 3 (bf16) or 6 (fp32) ring chunks
+    # and 11 or 21 512 B chunks, so the shares are uneven; Zipf routing, masks,
+    # and a ragged call
+    w = Workload("split", 8, 600, 2600, 16, 3, routing="zipf", zipf_s=1.2, mask_p=0.1)
+    full_check(Round(L, w, seed=7, tokens=tokens, dtype=dtype))
+
+
 def test_hot_expert_single_bucket(L):
     # every token of every rank picks expert 0: one bucket per source holds T rows
     w = WORKLOADS["skewed"].with_(H=256)
