@@ -61,6 +61,7 @@ struct Geometry {
   int32_t* err;          // optional error word
   uint32_t flags;        // LLMOE_FLAG_*
   int T_max, T, H, R, E, K, L;
+  uint32_t L_mul;  // ceil(2^32 / L) (0 for L = 1): e / L = umulhi(e, L_mul) for every expert id e < 2^16
   int dtype;      // LLMOE_DTYPE_*
   int row_bytes;  // H * element size
   int nq;       // 16-byte quads per row
@@ -205,11 +206,15 @@ __device__ void route_hist(const Geometry& g, const int64_t* __restrict__ idx, i
 __device__ __forceinline__ int route_slot(const Geometry& g, const RouteSmem& s, int q) {
   const int e = s.ent[q];
   if (e < 0) return -1;
-  const int K = g.K, tl = q / K, k = q % K;
-  int r = 0;
-  for (int p = 0; p < tl * K; ++p) r += (s.ent[p] == e);
-  for (int k2 = 0; k2 < k; ++k2)
-    if (s.ent[tl * K + k2] == e) report(g.err, LLMOE_DEV_DUPLICATE);
+  int r = 0, tl = 0, k = q;  // one token per CTA: entry q is the token's k-th
+  if (g.TB > 1) {
+    tl = q / g.K;
+    k = q - tl * g.K;
+    for (int p = 0; p < tl * g.K; ++p) r += (s.ent[p] == e);  // earlier tokens of the block
+  }
+  if (g.err != nullptr)  // validate mode: an expert twice in one token
+    for (int k2 = 0; k2 < k; ++k2)
+      if (s.ent[tl * g.K + k2] == e) report(g.err, LLMOE_DEV_DUPLICATE);
   const int sl = s.hist[e] + r;
   if (sl >= g.T_max) {  // only reachable when a token repeats an expert
     report(g.err, LLMOE_DEV_SLOT_RANGE);
@@ -222,6 +227,11 @@ __device__ __forceinline__ int route_slot(const Geometry& g, const RouteSmem& s,
 __device__ __forceinline__ void route_count_block(const RouteSmem& s, int nblock) {
   for (int q = threadIdx.x; q < nblock; q += blockDim.x)
     if (s.ent[q] >= 0) atomicAdd(&s.hist[s.ent[q]], 1);
+}
+
+// Owner of expert e: rank e / L, local expert e % L, without a division.
+__device__ __forceinline__ int owner_rank(const Geometry& g, int e) {
+  return g.L_mul == 0 ? e : (int)__umulhi((unsigned)e, g.L_mul);
 }
 
 // Zeroes the other buffer set's R * E signal words (LLMOE_FLAG_CLEAN_OTHER_SET:
@@ -539,7 +549,7 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
       const int e = s.ent[q], sl = route_slot(g, s, q);
       uintptr_t d = 0;
       if (sl >= 0) {
-        const int dst = e / g.L, le = e % g.L;
+        const int dst = owner_rank(g, e), le = e - dst * g.L;
         const uint64_t row = ((uint64_t)le * g.R + src) * g.T_max + sl;
         d = pack_dest(g.base + dst * g.rank_stride + g.recv_off + row * g.msg);
       }
@@ -1545,6 +1555,8 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   g->E = E;
   g->K = K;
   g->L = E / R;
+  // e / L as a multiply-high: exact for e < 2^16 because e * (L_mul * L - 2^32) < 2^32
+  g->L_mul = g->L == 1 ? 0u : (uint32_t)(((1ull << 32) + g->L - 1) / g->L);
   g->dtype = bs->dtype;
   g->row_bytes = H * es;
   g->nq = g->row_bytes / 16;
