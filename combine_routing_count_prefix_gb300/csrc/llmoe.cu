@@ -457,10 +457,6 @@ constexpr int kDspThreads = 32 * (1 + kDspConsumers);
 #ifndef LLMOE_CMB_SPLIT
 #define LLMOE_CMB_SPLIT 2
 #endif
-#ifndef LLMOE_DSP_DEST_REGS
-#define LLMOE_DSP_DEST_REGS 8
-#endif
-constexpr int kDestRegs = LLMOE_DSP_DEST_REGS > 0 ? LLMOE_DSP_DEST_REGS : 1;  // destinations a dispatch thread keeps in registers
 
 // Named barrier of the consumer warps of a dispatch CTA (the producer warp
 // streams x and does not take part in the route scan).
@@ -559,9 +555,6 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
     TRACE(3, threadIdx.x == 32);
     if (early) wait_prior_grid();  // the receive rows may be in use until now
     TRACE(4, threadIdx.x == 32);
-    const bool small_k = g.K <= kDestRegs;
-    uintptr_t dreg[kDestRegs];  // top-k <= kDestRegs: the token's destinations, kept across its chunks
-    int cached_tl = -1;
     int it = 0;
     for (; it < n_iters; ++it) {
       const int sidx = it % kDspStages;
@@ -570,26 +563,19 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
       const int tl = it / nch, c = c0 + it % nch;
       const int len = min(kDspChunk, row_bytes - c * kDspChunk);
       const uint8_t* sb = ring.stage(sidx);
+      // the token's destinations from shared memory, one put_quad in a loop:
+      // unrolling the destinations into registers made the loop's code so
+      // much larger that its first pass, from cold instruction caches, cost
+      // more than the loads it saved (tiny workload 0.9 us a round)
       const uintptr_t* dsts = s_dst + tl * g.K;
-      if (small_k && tl != cached_tl) {
-#pragma unroll
-        for (int k = 0; k < kDestRegs; ++k) dreg[k] = k < g.K ? dsts[k] : 0;
-        cached_tl = tl;
-      }
       if (ct * 16 < len) {
         const uint4 cur = *reinterpret_cast<const uint4*>(sb + 16 + 16 * ct);
         const uint4 prev = (c == 0 && ct == 0) ? make_uint4(0, 0, 0, (uint32_t)(t0 + tl))
                                                : *reinterpret_cast<const uint4*>(sb + 16 * ct);
         const int j = c * (kDspChunk / 16) + ct;
-        if (small_k) {
-#pragma unroll
-          for (int k = 0; k < kDestRegs; ++k)
-            if (dreg[k] != 0) put_quad(dreg[k], j, g.nq, prev, cur);
-        } else {
-          for (int k = 0; k < g.K; ++k) {
-            const uintptr_t d = dsts[k];
-            if (d != 0) put_quad(d, j, g.nq, prev, cur);
-          }
+        for (int k = 0; k < g.K; ++k) {
+          const uintptr_t d = dsts[k];
+          if (d != 0) put_quad(d, j, g.nq, prev, cur);
         }
       }
       __syncwarp();
@@ -687,13 +673,13 @@ __device__ __forceinline__ uint4 pack_q(const float (&acc)[8]) {
 
 constexpr int kCmbThreads = LLMOE_CMB_THREADS;
 constexpr int kCmbWarps = kCmbThreads / 32;
-constexpr int kKBatch = 8;
+constexpr int kKBatch = 8;  // most expert-row loads a lane has in flight
 
 // Grid: R count CTAs (count_source: the flag words), then R * nblk data CTAs.
 // A data CTA reduces tokens [t0, t1) of source rank src; one warp reduces 32
 // quads (512 B) of one output row per unit: up to kKBatch expert rows are
 // loaded (16 B per lane each) before they are accumulated, in ascending k.
-template <int DT>
+template <int DT, int KB>  // KB: expert-row loads in flight per lane, the top-k rounded up to 2, 4 or 8
 __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const void* __restrict__ y,
                                                               const int64_t* __restrict__ idx,
                                                               const float* __restrict__ topk_w,
@@ -750,16 +736,16 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
     const uint4* const* trows = s_row + tl * g.K;
     const float* tws = s_w + tl * g.K;
-    for (int k0 = 0; k0 < g.K; k0 += kKBatch) {
-      uint4 v[kKBatch];
+    for (int k0 = 0; k0 < g.K; k0 += KB) {
+      uint4 v[KB];
 #pragma unroll
-      for (int i = 0; i < kKBatch; ++i) {
+      for (int i = 0; i < KB; ++i) {
         const int k = k0 + i;
         v[i] = make_uint4(0, 0, 0, 0);
         if (k < g.K && trows[k] != nullptr) v[i] = ld_stream16(trows[k] + j);
       }
 #pragma unroll
-      for (int i = 0; i < kKBatch; ++i) {
+      for (int i = 0; i < KB; ++i) {
         const int k = k0 + i;
         if (k < g.K && trows[k] != nullptr) axpy_q<DT>(acc, tws[k], v[i]);
       }
@@ -1582,7 +1568,7 @@ void set_blocking(Geometry* g, int blocks_per_sm, int extra_ctas = 0) {
   g->nblk = g->T > 0 ? (g->T + g->TB - 1) / g->TB : 1;
 }
 
-constexpr int kMaxSlots = 32;  // kslot values: kernel id * 4 + payload type
+constexpr int kMaxSlots = 40;  // kslot values: kernel id * 4 + payload type
 std::atomic<int> g_smem_optin[kMaxDevices][kMaxSlots];
 
 // Opts a kernel in to more than 48 KB of dynamic shared memory (once per
@@ -1613,7 +1599,9 @@ enum KernelId {
   kCombineReduceKernel = 4,
   kUnpackKernel = 5,
   kSignaledKernel = 6,
-  kNumKernels = 7
+  kCombineKernel4 = 7,
+  kCombineKernel2 = 8,
+  kNumKernels = 9
 };
 // (dynamic shared memory bytes << 32 | resident CTAs per SM) of the last query
 std::atomic<uint64_t> g_occupancy[kMaxDevices][kMaxSlots];
@@ -1722,16 +1710,29 @@ unsigned count_and_data_ctas(const Geometry& g) {
   return (unsigned)(g.R + (g.T > 0 ? g.R * g.nblk * g.dsplit * g.csplit : 0));
 }
 
+template <int DT, int KB>
+int launch_combine_kb(Geometry& g, const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
+                      llmoe_stream_t stream) {
+  const int id = kslot(KB == kKBatch ? kCombineKernel : KB == 4 ? kCombineKernel4 : kCombineKernel2, DT);
+  const void* fn = (const void*)combine_kernel<DT, KB>;
+  set_blocking(&g, blocks_per_sm(id, fn, kCmbThreads, combine_smem_bytes(g)), g.R);
+  g.csplit = g.TB > 1 ? std::max(1, std::min(LLMOE_CMB_SPLIT, g.nchunks)) : 1;
+  const size_t smem = combine_smem_bytes(g);
+  const int rc = set_smem(id, fn, smem);
+  if (rc != LLMOE_SUCCESS) return rc;
+  return launch(combine_kernel<DT, KB>, count_and_data_ctas(g), kCmbThreads, smem, stream, g, y, topk_idx, topk_w,
+                out);
+}
+
+// The kernel whose unrolled load batch is the smallest that holds the
+// top-k (2, 4 or 8): with a small top-k the batch of 8 only adds code, and the
+// first pass through it, from cold instruction caches, costs time.
 template <int DT>
 int launch_combine(Geometry& g, const void* y, const int64_t* topk_idx, const float* topk_w, void* out,
                    llmoe_stream_t stream) {
-  const int id = kslot(kCombineKernel, DT);
-  set_blocking(&g, blocks_per_sm(id, (const void*)combine_kernel<DT>, kCmbThreads, combine_smem_bytes(g)), g.R);
-  g.csplit = g.TB > 1 ? std::max(1, std::min(LLMOE_CMB_SPLIT, g.nchunks)) : 1;
-  const size_t smem = combine_smem_bytes(g);
-  const int rc = set_smem(id, (const void*)combine_kernel<DT>, smem);
-  if (rc != LLMOE_SUCCESS) return rc;
-  return launch(combine_kernel<DT>, count_and_data_ctas(g), kCmbThreads, smem, stream, g, y, topk_idx, topk_w, out);
+  if (g.K <= 2) return launch_combine_kb<DT, 2>(g, y, topk_idx, topk_w, out, stream);
+  if (g.K <= 4) return launch_combine_kb<DT, 4>(g, y, topk_idx, topk_w, out, stream);
+  return launch_combine_kb<DT, kKBatch>(g, y, topk_idx, topk_w, out, stream);
 }
 
 template <int DT>
