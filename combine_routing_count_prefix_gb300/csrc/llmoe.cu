@@ -70,6 +70,7 @@ struct Geometry {
   int nblk;     // token blocks per source rank
   int dsplit;   // dispatch: data CTAs per token block (each a share of the rows' ring chunks)
   int csplit;   // combine: data CTAs per token block (each a share of the rows' 512 B chunks)
+  int pf_units; // combine: units per warp whose expert rows are prefetched into L2 before the wait
 };
 
 __device__ __forceinline__ void report(int32_t* err, int32_t code) {
@@ -436,6 +437,9 @@ __device__ void ring_drain(const Ring<kStages>& r, const RingState& st, int32_t*
 #ifndef LLMOE_CMB_THREADS
 #define LLMOE_CMB_THREADS 128
 #endif
+#ifndef LLMOE_CMB_PREFETCH_BYTES
+#define LLMOE_CMB_PREFETCH_BYTES (16 << 20)  // expert-row bytes a combine prefetches into L2 before its wait
+#endif
 
 constexpr int kDspConsumers = LLMOE_DSP_CONSUMERS;   // warps; lanes x 16 B = one chunk
 constexpr int kDspChunk = kDspConsumers * 32 * 16;   // x bytes per stage
@@ -721,7 +725,23 @@ __global__ void __launch_bounds__(kCmbThreads) combine_kernel(Geometry g, const 
   }
   __syncthreads();
   TRACE_C(3, threadIdx.x == 0);
-  if (early) wait_prior_grid();  // y may come from the previous kernel
+  if (early) {
+    // While the previous kernel drains, pull the expert rows of each warp's
+    // first units into L2.  A prefetch reads nothing into the kernel: if the
+    // previous kernel is still writing y, its stores update the same L2 lines
+    // (L2 is where the device's memory is kept coherent), and the loads below
+    // come after the wait.
+    const int nunits = (t1 - t0) * g.nchunks;
+    for (int u = warp; u < nunits && u < warp + g.pf_units * kCmbWarps; u += kCmbWarps) {
+      const int tl = u / g.nchunks, j = (u % g.nchunks) * 32 + lane;
+      if (j < g.nq)
+        for (int k = 0; k < g.K; ++k) {
+          const uint4* r = s_row[tl * g.K + k];
+          if (r != nullptr) asm volatile("prefetch.global.L2 [%0];" ::"l"(r + j));
+        }
+    }
+    wait_prior_grid();  // y may come from the previous kernel
+  }
   TRACE_C(4, threadIdx.x == 0);
 
   const int c0 = g.nchunks * part / g.csplit, cn = g.nchunks * (part + 1) / g.csplit - c0;  // this CTA's chunks
@@ -1558,6 +1578,7 @@ int make_geometry(const llmoe_buf_set_t* bs, bool need_buffers, Geometry* g) {
   g->nblk = T > 0 ? T : 1;
   g->dsplit = 1;
   g->csplit = 1;
+  g->pf_units = 1;
   return LLMOE_SUCCESS;
 }
 
@@ -1724,6 +1745,16 @@ int launch_combine_kb(Geometry& g, const void* y, const int64_t* topk_idx, const
   const void* fn = (const void*)combine_kernel<DT, KB>;
   set_blocking(&g, blocks_per_sm(id, fn, kCmbThreads, combine_smem_bytes(g)), g.R);
   g.csplit = g.TB > 1 ? std::max(1, std::min(LLMOE_CMB_SPLIT, g.nchunks)) : 1;
+  {
+    // the prefetch before the wait (LLMOE_FLAG_INPUTS_READY): about
+    // LLMOE_CMB_PREFETCH_BYTES of expert rows over the CTAs of the first wave,
+    // at least one unit per warp and at most four.  Measured on DS-V3 (16.8 MB
+    // per unit per warp over the grid): one unit saves 1.3 us a round, two 0.8,
+    // seven lose 2.7; many-small (4.2 MB per unit) gains from both its units.
+    const int64_t resident = std::min<int64_t>((int64_t)g.R * g.nblk * g.csplit, (int64_t)num_sms() * 8);
+    const int64_t per_unit = resident * kCmbWarps * g.K * 512;
+    g.pf_units = (int)std::max<int64_t>(1, std::min<int64_t>(4, LLMOE_CMB_PREFETCH_BYTES / std::max<int64_t>(per_unit, 1)));
+  }
   const size_t smem = combine_smem_bytes(g);
   const int rc = set_smem(id, fn, smem);
   if (rc != LLMOE_SUCCESS) return rc;
