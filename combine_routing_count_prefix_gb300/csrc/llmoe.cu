@@ -448,9 +448,9 @@ constexpr int kDspStages = LLMOE_DSP_STAGES;
 constexpr int kDspThreads = 32 * (1 + kDspConsumers);
 // A grid with several tokens per CTA (TB > 1: more tokens than one wave of
 // CTAs, e.g. 8 ranks x 1,024 tokens) is split further: each token block gets
-// up to LLMOE_DSP_SPLIT dispatch CTAs (one per 2 KB ring chunk of its rows) and
-// LLMOE_CMB_SPLIT combine CTAs, each moving a contiguous share of the rows'
-// chunks.  The grid then spans many waves and the CTA scheduler gives the SMs
+// up to LLMOE_DSP_SPLIT dispatch CTAs (one per 2 KB ring chunk of its rows) and,
+// from 4 tokens per block, LLMOE_CMB_SPLIT combine CTAs, each moving a
+// contiguous share of the rows' chunks.  The grid then spans many waves and the CTA scheduler gives the SMs
 // that move rows fastest more CTAs: a GB300's SMs do not move rows at one rate
 // (per-SM rates measured in the dispatch differ by up to 1.9x, in groups of
 // SMs), and with one wave of equal CTAs the slowest group sets the kernel's
@@ -1744,7 +1744,10 @@ int launch_combine_kb(Geometry& g, const void* y, const int64_t* topk_idx, const
   const int id = kslot(KB == kKBatch ? kCombineKernel : KB == 4 ? kCombineKernel4 : kCombineKernel2, DT);
   const void* fn = (const void*)combine_kernel<DT, KB>;
   set_blocking(&g, blocks_per_sm(id, fn, kCmbThreads, combine_smem_bytes(g)), g.R);
-  g.csplit = g.TB > 1 ? std::max(1, std::min(LLMOE_CMB_SPLIT, g.nchunks)) : 1;
+  // only for blocks of at least 4 tokens: with 2 (a grid of about two
+  // waves' tokens) the split leaves a part wave that costs more than it
+  // balances (dense16 combine 43.8 -> 46.1 us)
+  g.csplit = g.TB >= 4 ? std::max(1, std::min(LLMOE_CMB_SPLIT, g.nchunks)) : 1;
   {
     // the prefetch before the wait (LLMOE_FLAG_INPUTS_READY): about
     // LLMOE_CMB_PREFETCH_BYTES of expert rows over the CTAs of the first wave,
