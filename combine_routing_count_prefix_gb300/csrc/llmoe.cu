@@ -920,6 +920,174 @@ __device__ __forceinline__ uint4 ld_payload_quad(const uint8_t* pay, int phase, 
   return make_uint4(__ldg(w), __ldg(w + 1), __ldg(w + 2), __ldg(w + 3));
 }
 
+// Reduce through a shared-memory ring (combine_reduce_ring_kernel), for grids
+// with more than one unit per consumer warp.  A CTA takes a contiguous range of the
+// R * T * nchunks (token, 512 B chunk) units.  Its producer warp copies each
+// unit's K message chunks into one ring stage with cp.async.bulk, lane k the
+// chunk of entry k: the 16-byte-aligned span that covers the chunk (the
+// payload sits at a 4-byte phase, so one quad more when the phase is not
+// zero).  Consumer warp w takes the units at ring positions w, w + C, ...:
+// lane j reads quads j and j + 1 of each entry's span from shared memory,
+// shifts the payload words into place and accumulates them, ascending k.
+// The copies need no registers while in flight, so a CTA keeps kRedStages
+// units' messages in flight, where register loads held four.
+#ifndef LLMOE_RED_STAGES
+#define LLMOE_RED_STAGES 4
+#endif
+#ifndef LLMOE_RED_CONSUMERS
+#define LLMOE_RED_CONSUMERS 2
+#endif
+#ifndef LLMOE_RED_WIDTH
+#define LLMOE_RED_WIDTH 1
+#endif
+constexpr int kRedStages = LLMOE_RED_STAGES;
+constexpr int kRedConsumers = LLMOE_RED_CONSUMERS;
+constexpr int kRedThreads = 32 * (1 + kRedConsumers);
+constexpr int kRedWidth = LLMOE_RED_WIDTH;  // 512 B chunks per unit
+constexpr int kRedSlot = (32 * kRedWidth + 1) * 16;  // one entry's span: the unit's payload quads and the one the phase spills into
+// Stage s is used only by consumer warp s % kRedConsumers, so a consumer's
+// parity waits on a stage follow each other in order; with a stage shared by
+// two consumers, one could wait for a phase two ahead of the barrier's and
+// take the parity of an old phase for its own.
+static_assert(kRedStages % kRedConsumers == 0, "every ring stage belongs to one consumer warp");
+
+struct RedMeta {
+  int phase;  // the payload's 4-byte phase; -1: masked entry
+  float w;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(kRedThreads) combine_reduce_ring_kernel(Geometry g, const int64_t* __restrict__ idx,
+                                                                          const float* __restrict__ topk_w,
+                                                                          void* __restrict__ out) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int K = g.K;
+  uint8_t* data = smem;  // [stage][k][kRedSlot]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kRedStages * K * kRedSlot);
+  uint64_t* empty = full + kRedStages;
+  RedMeta* meta = reinterpret_cast<RedMeta*>(empty + kRedStages);  // [stage][k]
+  int64_t* unit_tok = reinterpret_cast<int64_t*>(meta + kRedStages * K);  // [stage]
+  __shared__ int s_stop[kRedConsumers];  // per consumer warp: the first position it did not consume
+  __shared__ int s_issued;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRedStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init_fence();
+    s_issued = 0;
+  }
+  release_next_grid();
+  wait_prior_grid();
+  __syncthreads();
+  const int nu = (g.nchunks + kRedWidth - 1) / kRedWidth;  // units per token
+  const int64_t nunits = (int64_t)g.R * g.T * nu;
+  const int64_t ubeg = nunits * blockIdx.x / gridDim.x, uend = nunits * (blockIdx.x + 1) / gridDim.x;
+  const int npos = (int)(uend - ubeg);
+
+  if (warp == 0) {
+    // producer: lanes k < K hold entry k's expert id and weight of the current token
+    int64_t tok = ubeg / nu;
+    int c = (int)(ubeg - tok * nu);
+    int src = (int)(tok / g.T), t = (int)(tok - (int64_t)src * g.T);
+    long long e_lane = -1;
+    float w_lane = 0.0f;
+    bool fresh = true, ok = true;
+    int pos = 0;
+    for (; pos < npos; ++pos) {
+      if (fresh) {
+        e_lane = -1;
+        w_lane = 0.0f;
+        if (lane < K) {
+          e_lane = idx[tok * K + lane];
+          w_lane = topk_w[tok * K + lane];
+        }
+        fresh = false;
+      }
+      const int sidx = pos % kRedStages, use = pos / kRedStages;
+      if (lane == 0 && use > 0) ok = mbar_wait(&empty[sidx], (use - 1) & 1, g.err);
+      ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+      if (!ok) break;
+      const int len = min(512 * kRedWidth, g.row_bytes - 512 * kRedWidth * c);
+      const bool valid = lane < K && e_lane >= 0 && e_lane < g.E;
+      uint32_t bytes = 0;
+      int phase = -1;
+      const uint8_t* span = nullptr;
+      if (valid) {
+        const uint8_t* msg = g.base + src * g.rank_stride + g.recv_off + ((uint64_t)e_lane * g.T_max + t) * g.msg;
+        const uint8_t* p = msg + 4 + 512 * kRedWidth * (size_t)c;
+        phase = (int)((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+        span = p - 4 * phase;
+        bytes = (uint32_t)len + (phase != 0 ? 16u : 0u);
+        if (g.err != nullptr && c == 0 && *reinterpret_cast<const int32_t*>(msg) != t)
+          report(g.err, LLMOE_DEV_BAD_MESSAGE);
+      }
+      if (lane < K) meta[sidx * K + lane] = RedMeta{phase, w_lane};
+      if (lane == 0) unit_tok[sidx] = tok;
+      uint32_t total = bytes;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[sidx], total);
+      __syncwarp();
+      if (valid) bulk_load(data + ((size_t)sidx * K + lane) * kRedSlot, span, bytes, &full[sidx]);
+      if (++c == nu) {
+        c = 0;
+        ++tok;
+        if (++t == g.T) {
+          t = 0;
+          ++src;
+        }
+        fresh = true;
+      }
+    }
+    if (lane == 0) s_issued = pos;
+    __syncwarp();
+  } else {
+    const int cw = warp - 1;
+    int pos = cw;
+    for (; pos < npos; pos += kRedConsumers) {
+      const int sidx = pos % kRedStages;
+      if (!mbar_wait(&full[sidx], (pos / kRedStages) & 1, g.err)) break;
+      const int64_t tok = unit_tok[sidx];
+      const int c = (int)((ubeg + pos) - tok * nu);
+      uint4* orow = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(out) + tok * g.row_bytes);
+#pragma unroll
+      for (int i = 0; i < kRedWidth; ++i) {
+        const int j = (c * kRedWidth + i) * 32 + lane;
+        if (j >= g.nq) break;
+        float acc[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) acc[a] = 0.0f;
+        const uint4* q = reinterpret_cast<const uint4*>(data + (size_t)sidx * K * kRedSlot) + 32 * i + lane;
+        for (int k = 0; k < K; ++k, q += kRedSlot / 16) {  // ascending k
+          const RedMeta m = meta[sidx * K + k];
+          if (m.phase >= 0) axpy_q<DT>(acc, m.w, unshift_words(q[0], q[1], m.phase));
+        }
+        orow[j] = pack_q<DT>(acc);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sidx]);
+    }
+    if (lane == 0) s_stop[cw] = pos;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {  // after a timeout: wait (bounded) for the copies nobody consumed
+    for (int p = max(0, s_issued - kRedStages); p < s_issued; ++p)
+      if (p >= s_stop[p % kRedConsumers] && !mbar_wait(&full[p % kRedStages], (p / kRedStages) & 1, g.err)) break;
+  }
+}
+
+size_t reduce_smem_bytes(const Geometry& g) {
+  return (size_t)kRedStages * g.K * kRedSlot + 2 * kRedStages * sizeof(uint64_t) +
+         (size_t)kRedStages * g.K * sizeof(RedMeta) + kRedStages * sizeof(int64_t);
+}
+
+// Reduce with register loads (combine_reduce_kernel), for smaller grids:
+// there a unit's latency is the kernel's, and the ring's producer hand-off
+// adds to it (many-small staged combine 14.4 us this way, 16.3 us through the
+// ring).
 #ifndef LLMOE_REDUCE_KBATCH
 #define LLMOE_REDUCE_KBATCH 4
 #endif
@@ -1003,6 +1171,7 @@ __global__ void __launch_bounds__(kThreads, 4) combine_reduce_kernel(Geometry g,
     }
   }
 }
+
 
 // ---------------------------------------------------------------------------
 // unpack, and the dispatch whose CTAs signal each other
@@ -1629,7 +1798,8 @@ enum KernelId {
   kSignaledKernel = 6,
   kCombineKernel4 = 7,
   kCombineKernel2 = 8,
-  kNumKernels = 9
+  kCombineReduceRingKernel = 9,
+  kNumKernels = 10
 };
 // (dynamic shared memory bytes << 32 | resident CTAs per SM) of the last query
 std::atomic<uint64_t> g_occupancy[kMaxDevices][kMaxSlots];
@@ -1778,10 +1948,25 @@ int launch_combine(Geometry& g, const void* y, const int64_t* topk_idx, const fl
 
 template <int DT>
 int launch_reduce(const Geometry& g, const int64_t* topk_idx, const float* topk_w, void* out, llmoe_stream_t stream) {
-  const int64_t warps = (int64_t)g.R * g.T * g.nchunks;
+  // the ring kernel when a full wave of it has more than one unit per consumer
+  // warp (skewed: 1.6, staged combine 37.2 -> 35.3 us; many-small: 0.64, where
+  // it took 16.3 us against 14.4)
+  const int64_t ring_units = (int64_t)g.R * g.T * ((g.nchunks + kRedWidth - 1) / kRedWidth);
+  const size_t smem = reduce_smem_bytes(g);
+  int rc = set_smem(kslot(kCombineReduceRingKernel, DT), (const void*)combine_reduce_ring_kernel<DT>, smem);
+  if (rc != LLMOE_SUCCESS) return rc;
+  const int64_t ring_wave = (int64_t)num_sms() * blocks_per_sm(kslot(kCombineReduceRingKernel, DT),
+                                                               (const void*)combine_reduce_ring_kernel<DT>,
+                                                               kRedThreads, smem);
+  if (ring_units > ring_wave * kRedConsumers) {
+    // one wave, each CTA a contiguous range of units
+    return launch(combine_reduce_ring_kernel<DT>, (unsigned)ring_wave, kRedThreads, smem, stream, g, topk_idx, topk_w,
+                  out);
+  }
+  const int64_t units = (int64_t)g.R * g.T * g.nchunks;
   const int64_t wave = (int64_t)num_sms() * blocks_per_sm(kslot(kCombineReduceKernel, DT),
                                                           (const void*)combine_reduce_kernel<DT>, kThreads, 0);
-  const int64_t blocks = std::min<int64_t>(wave, (warps + kThreads / 32 - 1) / (kThreads / 32));
+  const int64_t blocks = std::min<int64_t>(wave, (units + kThreads / 32 - 1) / (kThreads / 32));
   return launch(combine_reduce_kernel<DT>, (unsigned)blocks, kThreads, 0, stream, g, topk_idx, topk_w, out);
 }
 

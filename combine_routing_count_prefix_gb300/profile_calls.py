@@ -14,7 +14,8 @@ Kernels per call: route -> route_kernel; clean -> clean_kernel; dispatch ->
 dispatch_kernel; combine -> combine_kernel<payload type>; unpack ->
 unpack_balanced_kernel (fewer buckets than routed entries) or unpack_kernel
 (otherwise, e.g. many_small); signaled -> dispatch_signaled_kernel; staged ->
-combine_put_kernel, combine_reduce_kernel.  Each call that reads a dispatch's
+combine_put_kernel, then combine_reduce_ring_kernel (more (token, chunk) units
+than consumer warps in a full wave, e.g. dense16) or combine_reduce_kernel.  Each call that reads a dispatch's
 results gets one, outside the flush.
 """
 from __future__ import annotations

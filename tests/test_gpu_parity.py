@@ -499,6 +499,19 @@ def test_staged_combine_shapes(L, R, E, K, H, T):
     run_staged(L, Round(L, w, seed=R + E + K + H + T))
 
 
+# Sizes at which the reduce runs through its shared-memory ring (more (token,
+# chunk) units than consumer warps in a full wave): rows with a partial last
+# 512 B chunk, masked entries, the largest top-k, fp16 / fp32 payloads and a
+# call with fewer tokens than the layout holds.
+@pytest.mark.parametrize("R,E,K,H,T,tokens,dtype", [(4, 12, 5, 1000, 500, None, "bf16"),
+                                                    (2, 64, 32, 520, 300, None, "bf16"),
+                                                    (4, 8, 3, 260, 1000, 999, "fp32"),
+                                                    (8, 16, 4, 1032, 250, None, "fp16")])
+def test_staged_combine_ring_shapes(L, R, E, K, H, T, tokens, dtype):
+    w = Workload("staged_ring", R, T, H, E, K, mask_p=0.3)
+    run_staged(L, Round(L, w, seed=R + E + K + H + T + 7, tokens=tokens, dtype=dtype))
+
+
 def test_staged_combine_fewer_tokens_and_set_one(L):
     w = WORKLOADS["dsv3"].with_(H=1024)
     run_staged(L, Round(L, w, seed=33, tokens=77, dispatch_set=1))
