@@ -773,6 +773,20 @@ def run_signaled(args, llmoe, w, x, idx, rb, es, flush, steps: int = 200):
     return res
 
 
+def pack_e2e_input(inp):
+    """x, topk_idx and topk_w of one step laid end to end in one pinned host
+    buffer (uint8), the layout the e2e step uploads in one copy."""
+    import torch
+
+    parts = [np.ascontiguousarray(inp[k]).view(np.uint8).reshape(-1) for k in ("x", "topk_idx", "topk_w")]
+    hin = torch.empty(sum(p.size for p in parts), dtype=torch.uint8).pin_memory()
+    off = 0
+    for p in parts:
+        hin[off:off + p.size].copy_(torch.from_numpy(p))
+        off += p.size
+    return hin
+
+
 def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
     """Rounds through the C ABI with host buffers, per step: the inputs copied
     from pinned host memory, the result (the combine output) read back.
@@ -790,10 +804,7 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
 
     x, idx, wts = inp["x"], inp["topk_idx"], inp["topk_w"]
     x_b, idx_b, w_b = x.nbytes, idx.nbytes, wts.nbytes  # x: whole 16-byte rows; idx: 8-byte words
-    hin = torch.empty(x_b + idx_b + w_b, dtype=torch.uint8).pin_memory()
-    hin[:x_b].copy_(torch.from_numpy(np.ascontiguousarray(x).view(np.uint8).reshape(-1)))
-    hin[x_b:x_b + idx_b].copy_(torch.from_numpy(np.ascontiguousarray(idx).view(np.uint8).reshape(-1)))
-    hin[x_b + idx_b:].copy_(torch.from_numpy(np.ascontiguousarray(wts).view(np.uint8).reshape(-1)))
+    hin = pack_e2e_input(inp)
     din = torch.empty_like(hin, device="cuda")
     pay = torch.float32 if rb.msg_bytes - 4 == 4 * w.H else torch.int16
     dx = din[:x_b].view(pay).view(w.R, tokens, w.H)
@@ -833,7 +844,7 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
     us, n = timed(layer)
     serial = {"value": round(us, 2), "unit": "us/round", "steps": n,
               "note": "the same layer with each step's copies and kernels one after another on one stream"}
-    pipe = run_e2e_pipelined(args, llmoe, w, hin, hout, rb, tokens, stream)
+    pipe = run_e2e_pipelined(args, llmoe, w, [hin], [hout], rb, tokens, stream)
     ceil = copy_ceiling(hin, hout)
     res = {"value": pipe["value"], "unit": "us/round", "h2d_bytes_per_step": hin.numel(),
            "d2h_bytes_per_step": d2h, "steps": pipe["steps"], "launches_per_step": 3,
@@ -889,15 +900,24 @@ def copy_ceiling(hin, hout, reps: int = 20) -> dict:
     return res
 
 
-def run_e2e_pipelined(args, llmoe, w, hin, hout, rb, tokens, stream):
-    """The e2e layer, steps back to back with their copies overlapped: step
-    i's upload (its own stream, into input buffer i % 2) waits only for the
-    kernels of step i-2 that read that buffer; step i's kernels wait for its
-    upload and for the download of step i-2 from output buffer i % 2; step
-    i's download (its own stream) waits for its kernels.  The kernels stay on
-    one stream in order (consecutive steps share the rank buffers)."""
+def run_e2e_pipelined(args, llmoe, w, hins, houts, rb, tokens, stream):
+    """The e2e layer, steps back to back with their copies overlapped; step i
+    uploads hins[i % len(hins)] and downloads into houts[i % len(houts)]
+    (pinned host buffers of one size each).  Step i's upload (its own stream,
+    into input buffer i % 2) waits only for the kernels of step i-2 that read
+    that buffer; step i's kernels wait for its upload and for the download of
+    step i-2 from output buffer i % 2; step i's download (its own stream)
+    waits for its kernels.  The kernels stay on one stream in order:
+    consecutive steps share the rank buffers, and one stream keeps each
+    kernel's launch behind its predecessor's drain (programmatic dependent
+    launch) with the cleans fused into the data kernels.  Kernels of
+    consecutive steps on two streams, each step on its own buffer set, took
+    108 us a layer against 103-105 this way: the cleans that schedule needs,
+    and launches no longer hidden behind a predecessor, cost more than the
+    overlap gained."""
     import torch
 
+    hin, hout = hins[0], houts[0]
     x_b = w.R * tokens * w.H * (hout.element_size())
     idx_b = w.R * tokens * w.K * 8
     pay = hout.dtype
@@ -924,7 +944,7 @@ def run_e2e_pipelined(args, llmoe, w, hin, hout, rb, tokens, stream):
             with torch.cuda.stream(s_up):
                 if i >= 2:
                     s_up.wait_event(comp_done[b])
-                din[b].copy_(hin, non_blocking=True)
+                din[b].copy_(hins[i % len(hins)], non_blocking=True)
                 up_done[b].record(s_up)
             stream.wait_event(up_done[b])
             if i >= 2:
@@ -936,9 +956,11 @@ def run_e2e_pipelined(args, llmoe, w, hin, hout, rb, tokens, stream):
             comp_done[b].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(comp_done[b])
-                hout.copy_(dout[b], non_blocking=True)
+                houts[i % len(houts)].copy_(dout[b], non_blocking=True)
                 down_done[b].record(s_down)
 
+    for s in (s_up, s_down):
+        s.wait_stream(stream)
     llmoe.llmoe_clean(rb.buf_set(0, w.K), stream)
     run(4)
     torch.cuda.synchronize()
@@ -951,12 +973,14 @@ def run_e2e_pipelined(args, llmoe, w, hin, hout, rb, tokens, stream):
     b_.record(s_down)
     torch.cuda.synchronize()
     us = a.elapsed_time(b_) * 1e3 / n
-    # the copies alone, as this schedule issues them (for the overlap achieved)
+    # the copies alone, as this schedule issues them (for the overlap achieved),
+    # into a host buffer of their own so the steps' outputs stay as they are
+    hscratch = torch.empty_like(hout).pin_memory()
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     c0.record(stream)
     for i in range(n):
         din[i % 2].copy_(hin, non_blocking=True)
-        hout.copy_(dout[i % 2], non_blocking=True)
+        hscratch.copy_(dout[i % 2], non_blocking=True)
     c1.record(stream)
     torch.cuda.synchronize()
     return {"value": round(us, 2), "steps": n, "copy_us_per_step": c0.elapsed_time(c1) * 1e3 / n}

@@ -43,3 +43,36 @@ def test_bench_line_on_tiny():
         for key in ("round_us", "dispatch_us", "combine_us", "effective_gbs", "frac_of_measured_hbm", "shape"):
             assert key in c, (name, key)
         assert c["round_us"] > 0 and c["dispatch_us"] > 0 and c["combine_us"] > 0
+
+
+@pytest.mark.gpu
+def test_e2e_schedule_matches_oracle_every_step():
+    # the bench's e2e schedule (double-buffered uploads and downloads on their
+    # own streams around the kernels) with a different input every step:
+    # each step's output is the oracle's identity-expert layer for that step's
+    # input, so no copy overwrote a buffer that a kernel still read
+    import types
+
+    import numpy as np
+    import torch
+
+    import bench
+    import oracle
+    from combine_routing_count_prefix_gb300 import llmoe
+    from combine_routing_count_prefix_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS["skewed"]
+    inps = [make_inputs(w, seed=s) for s in (3, 4, 5)]
+    hins = [bench.pack_e2e_input(inp) for inp in inps]
+    steps = 6
+    houts = [torch.empty((w.R, w.T, w.H), dtype=torch.int16).pin_memory() for _ in range(steps)]
+    rb = llmoe.RankBuffers(w.T, w.H, w.R, w.E, fill=0xA5)
+    args = types.SimpleNamespace(e2e_steps=steps)
+    bench.run_e2e_pipelined(args, llmoe, w, hins, houts, rb, w.T, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    for i in range(steps):
+        inp = inps[i % len(inps)]
+        u = oracle.unpack(inp["x"], inp["topk_idx"], w.E, num_max_tokens=w.T)
+        ref, _ = oracle.combine(u["recv_x"], inp["topk_idx"], inp["topk_w"], w.H, w.E, num_max_tokens=w.T)
+        got = houts[i].numpy().view(np.uint16)
+        assert np.array_equal(got, ref), f"step {i}: {int((got != ref).sum())} elements differ"
