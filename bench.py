@@ -735,7 +735,8 @@ def run_pipeline(args, llmoe, w, x, idx, wt, y, rb, tokens, es, micro_batches: i
 
 def run_signaled(args, llmoe, w, x, idx, rb, es, flush, steps: int = 200):
     """Dispatch plus unpack (received rows in the experts' input order): two
-    launches (llmoe_dispatch, llmoe_unpack) against one cooperative launch
+    launches (llmoe_dispatch, llmoe_unpack); the dispatch that writes the rows
+    itself (llmoe_dispatch_unpack, one launch); and one cooperative launch
     whose CTAs signal each other through the count words
     (llmoe_dispatch_signaled, bounded waits).  L2 flushed before each."""
     import torch
@@ -754,8 +755,12 @@ def run_signaled(args, llmoe, w, x, idx, rb, es, flush, steps: int = 200):
     def one_launch():
         llmoe.llmoe_dispatch_signaled(x, idx, recv_x, recv_src, ws, 2_000_000_000, bs, cur)
 
+    def with_rows():
+        llmoe.llmoe_dispatch_unpack(x, idx, recv_x, recv_src, bs, cur)
+
     res = {}
-    for name, fn in (("dispatch_then_unpack_us", two_launches), ("signaled_us", one_launch)):
+    for name, fn in (("dispatch_then_unpack_us", two_launches), ("dispatch_unpack_us", with_rows),
+                     ("signaled_us", one_launch)):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for i in range(steps + 3):
             flush()
@@ -769,6 +774,7 @@ def run_signaled(args, llmoe, w, x, idx, rb, es, flush, steps: int = 200):
         res[name] = round(statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3, 3)
     res["steps"] = steps
     res["note"] = ("events around the dispatch (+ unpack) only; the clean before each is outside; "
+                   "dispatch_unpack: one launch that writes the messages, the counts and the experts' input rows; "
                    "signaled: one cooperative launch, consumers wait on the count words with a clock limit")
     return res
 
@@ -792,12 +798,12 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
     from pinned host memory, the result (the combine output) read back.
 
     e2e: one MoE layer with identity experts.  x, topk_idx and topk_w sit in
-    one pinned host buffer and go up in one copy; llmoe_dispatch (set 0), then
-    llmoe_unpack lays the received rows out as the experts' input, in the
-    receive-row order the combine reads its expert outputs in, and an identity
-    expert's output is its input, so those rows are the combine's y;
-    llmoe_combine (set 1) returns bf16(sum_k w_k x) per token, and the output
-    comes back in one copy.
+    one pinned host buffer and go up in one copy; llmoe_dispatch_unpack (set
+    0) writes the messages and counts and lays the received rows out as the
+    experts' input, in the receive-row order the combine reads its expert
+    outputs in, and an identity expert's output is its input, so those rows
+    are the combine's y; llmoe_combine (set 1) returns bf16(sum_k w_k x) per
+    token, and the output comes back in one copy.
     e2e_dense_y: the bench round (dispatch + combine) with the dense expert
     outputs y [E*R*T, H] also copied from the host every step."""
     import torch
@@ -822,8 +828,7 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
 
     def layer():
         din.copy_(hin, non_blocking=True)
-        llmoe.llmoe_dispatch(dx, didx, bs0, stream)
-        llmoe.llmoe_unpack(recv_x, recv_src, bs0, stream)
+        llmoe.llmoe_dispatch_unpack(dx, didx, recv_x, recv_src, bs0, stream)
         llmoe.llmoe_combine(recv_x, didx, dw, dout, bs1, stream)
         hout.copy_(dout, non_blocking=True)
 
@@ -847,11 +852,11 @@ def run_e2e(args, llmoe, w, inp, dense_y, rb, tokens, stream):
     pipe = run_e2e_pipelined(args, llmoe, w, [hin], [hout], rb, tokens, stream)
     ceil = copy_ceiling(hin, hout)
     res = {"value": pipe["value"], "unit": "us/round", "h2d_bytes_per_step": hin.numel(),
-           "d2h_bytes_per_step": d2h, "steps": pipe["steps"], "launches_per_step": 3,
+           "d2h_bytes_per_step": d2h, "steps": pipe["steps"], "launches_per_step": 2,
            "note": "one MoE layer with identity experts through the C ABI, steps back to back: x, topk_idx, topk_w "
-                   "copied host->device in one copy from one pinned buffer; llmoe_dispatch; llmoe_unpack (the "
-                   "experts' input rows, which identity experts return as their output y); llmoe_combine over "
-                   "them; the output copied back.  Uploads and downloads run on their own streams into double "
+                   "copied host->device in one copy from one pinned buffer; llmoe_dispatch_unpack (the messages, "
+                   "counts and the experts' input rows, which identity experts return as their output y); "
+                   "llmoe_combine over them; the output copied back.  Uploads and downloads run on their own streams into double "
                    "buffers, so step i+1's upload and step i-1's download overlap step i's kernels; value = time "
                    "from the first upload to the last download / steps",
            "serial": serial, "copy_ceiling": ceil,
@@ -950,8 +955,7 @@ def run_e2e_pipelined(args, llmoe, w, hins, houts, rb, tokens, stream):
             if i >= 2:
                 stream.wait_event(down_done[b])
             dx, didx, dw = views[b]
-            llmoe.llmoe_dispatch(dx, didx, bs0, stream)
-            llmoe.llmoe_unpack(recv_x, recv_src, bs0, stream)
+            llmoe.llmoe_dispatch_unpack(dx, didx, recv_x, recv_src, bs0, stream)
             llmoe.llmoe_combine(recv_x, didx, dw, dout[b], bs1, stream)
             comp_done[b].record(stream)
             with torch.cuda.stream(s_down):

@@ -474,8 +474,15 @@ __device__ __forceinline__ void consumers_sync() {
 // the start.  The consumer warps meanwhile run the route scan among
 // themselves (named barrier) and pack the destinations into shared memory,
 // then take the ring's chunks.
+// kRows: the CTA also writes each entry's row of the experts' input, recv_x
+// row (e * R + src) * T_max + slot and recv_src there = t, which is what
+// llmoe_unpack makes from the messages: the CTA holds the row and knows the
+// slot, so it stores the row as it is (aligned) beside the message.
+template <bool kRows>
 __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, const void* __restrict__ x,
-                                                               const int64_t* __restrict__ idx) {
+                                                               const int64_t* __restrict__ idx,
+                                                               void* __restrict__ recv_x,
+                                                               int32_t* __restrict__ recv_src) {
   extern __shared__ __align__(128) unsigned char smem[];
   Ring<kDspStages> ring;
   ring.data = smem;
@@ -485,6 +492,7 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
   __shared__ RingState st;
   const RouteSmem s = carve_route(reinterpret_cast<unsigned char*>(ring.empty + kDspStages), g);
   uintptr_t* s_dst = reinterpret_cast<uintptr_t*>(s.slot + g.TB * g.K + (g.E & 1));
+  uint4** s_xrow = reinterpret_cast<uint4**>(s_dst + g.TB * g.K);  // kRows: the entries' recv_x rows
   const bool early = (g.flags & LLMOE_FLAG_INPUTS_READY) != 0;
   if ((int)blockIdx.x < g.R) {
     count_source(g, idx, blockIdx.x, s, early, true);
@@ -548,12 +556,19 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
     for (int q = ct; q < nblock; q += kDspConsumers * 32) {
       const int e = s.ent[q], sl = route_slot(g, s, q);
       uintptr_t d = 0;
+      uint4* xr = nullptr;
       if (sl >= 0) {
         const int dst = owner_rank(g, e), le = e - dst * g.L;
         const uint64_t row = ((uint64_t)le * g.R + src) * g.T_max + sl;
         d = pack_dest(g.base + dst * g.rank_stride + g.recv_off + row * g.msg);
+        if constexpr (kRows) {
+          const int64_t orow = ((int64_t)e * g.R + src) * g.T_max + sl;
+          xr = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(recv_x) + orow * row_bytes);
+          if (part == 0) recv_src[orow] = t0 + q / g.K;
+        }
       }
       s_dst[q] = d;
+      if constexpr (kRows) s_xrow[q] = xr;
     }
     consumers_sync();
     TRACE(3, threadIdx.x == 32);
@@ -580,6 +595,10 @@ __global__ void __launch_bounds__(kDspThreads, 8) dispatch_kernel(Geometry g, co
         for (int k = 0; k < g.K; ++k) {
           const uintptr_t d = dsts[k];
           if (d != 0) put_quad(d, j, g.nq, prev, cur);
+          if constexpr (kRows) {
+            uint4* xr = s_xrow[tl * g.K + k];
+            if (xr != nullptr) xr[j] = cur;
+          }
         }
       }
       __syncwarp();
@@ -1769,7 +1788,7 @@ void set_blocking(Geometry* g, int blocks_per_sm, int extra_ctas = 0) {
   g->nblk = g->T > 0 ? (g->T + g->TB - 1) / g->TB : 1;
 }
 
-constexpr int kMaxSlots = 40;  // kslot values: kernel id * 4 + payload type
+constexpr int kMaxSlots = 44;  // kslot values: kernel id * 4 + payload type
 std::atomic<int> g_smem_optin[kMaxDevices][kMaxSlots];
 
 // Opts a kernel in to more than 48 KB of dynamic shared memory (once per
@@ -1803,7 +1822,8 @@ enum KernelId {
   kCombineKernel4 = 7,
   kCombineKernel2 = 8,
   kCombineReduceRingKernel = 9,
-  kNumKernels = 10
+  kDispatchRowsKernel = 10,
+  kNumKernels = 11
 };
 // (dynamic shared memory bytes << 32 | resident CTAs per SM) of the last query
 std::atomic<uint64_t> g_occupancy[kMaxDevices][kMaxSlots];
@@ -1839,9 +1859,9 @@ size_t route_smem_bytes(const Geometry& g) {
   return sizeof(int) * ((size_t)g.E + 2 * tbk + (size_t)(g.E & 1));  // pad: 8-byte arrays follow
 }
 
-size_t dispatch_smem_bytes(const Geometry& g) {
+size_t dispatch_smem_bytes(const Geometry& g, bool rows = false) {
   return (size_t)kDspStages * kDspStageBytes + 2 * kDspStages * sizeof(uint64_t) + route_smem_bytes(g) +
-         sizeof(uintptr_t) * (size_t)g.TB * g.K;
+         sizeof(uintptr_t) * (size_t)g.TB * g.K * (rows ? 2 : 1);
 }
 
 size_t combine_smem_bytes(const Geometry& g) {
@@ -1910,6 +1930,22 @@ int static_counters(int32_t** out) {
 // when the call has no tokens).
 unsigned count_and_data_ctas(const Geometry& g) {
   return (unsigned)(g.R + (g.T > 0 ? g.R * g.nblk * g.dsplit * g.csplit : 0));
+}
+
+// The dispatch launch, with (kRows) or without the experts' input rows.
+template <bool kRows>
+int launch_dispatch(Geometry& g, const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src,
+                    llmoe_stream_t stream) {
+  const void* fn = (const void*)dispatch_kernel<kRows>;
+  const int id = kslot(kRows ? kDispatchRowsKernel : kDispatchKernel);
+  set_blocking(&g, blocks_per_sm(id, fn, kDspThreads, dispatch_smem_bytes(g, kRows)), g.R);
+  const int nch_row = (g.row_bytes + kDspChunk - 1) / kDspChunk;
+  g.dsplit = g.TB > 1 ? std::max(1, std::min(LLMOE_DSP_SPLIT, nch_row)) : 1;
+  const size_t smem = dispatch_smem_bytes(g, kRows);
+  int rc = set_smem(id, fn, smem);
+  if (rc != LLMOE_SUCCESS) return rc;
+  return launch(dispatch_kernel<kRows>, count_and_data_ctas(g), kDspThreads, smem, stream, g, x, topk_idx, recv_x,
+                recv_src);
 }
 
 template <int DT, int KB>
@@ -2101,13 +2137,19 @@ int llmoe_dispatch(const void* x, const int64_t* topk_idx, const llmoe_buf_set_t
   if (rc != LLMOE_SUCCESS) return rc;
   if (g.T > 0 && (x == nullptr || topk_idx == nullptr || !aligned(x, 16) || !aligned(topk_idx, 8)))
     return LLMOE_ERR_INVALID_ARGUMENT;
-  set_blocking(&g, blocks_per_sm(kslot(kDispatchKernel), (const void*)dispatch_kernel, kDspThreads, dispatch_smem_bytes(g)),
-               g.R);
-  const int nch_row = (g.row_bytes + kDspChunk - 1) / kDspChunk;
-  g.dsplit = g.TB > 1 ? std::max(1, std::min(LLMOE_DSP_SPLIT, nch_row)) : 1;
-  const size_t smem = dispatch_smem_bytes(g);
-  if ((rc = set_smem(kslot(kDispatchKernel), (const void*)dispatch_kernel, smem)) != LLMOE_SUCCESS) return rc;
-  return launch(dispatch_kernel, count_and_data_ctas(g), kDspThreads, smem, stream, g, x, topk_idx);
+  return launch_dispatch<false>(g, x, topk_idx, nullptr, nullptr, stream);
+}
+
+int llmoe_dispatch_unpack(const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src,
+                          const llmoe_buf_set_t* bs, llmoe_stream_t stream) {
+  Geometry g;
+  int rc = make_geometry(bs, true, &g);
+  if (rc != LLMOE_SUCCESS) return rc;
+  if (g.T > 0 && (x == nullptr || topk_idx == nullptr || !aligned(x, 16) || !aligned(topk_idx, 8)))
+    return LLMOE_ERR_INVALID_ARGUMENT;
+  if (recv_x == nullptr || recv_src == nullptr || !aligned(recv_x, 16) || !aligned(recv_src, 4))
+    return LLMOE_ERR_INVALID_ARGUMENT;
+  return launch_dispatch<true>(g, x, topk_idx, recv_x, recv_src, stream);
 }
 
 int llmoe_combine(const void* y, const int64_t* topk_idx, const float* topk_w, void* out,

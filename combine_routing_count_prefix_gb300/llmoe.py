@@ -48,6 +48,7 @@ LLMOE_MAX_EXPERTS = 8192
 
 EXPORTS = ("llmoe_layout_bytes", "llmoe_layout_bytes_dtype", "llmoe_layout_offsets", "llmoe_layout_offsets_dtype",
            "llmoe_route", "llmoe_dispatch", "llmoe_combine", "llmoe_combine_staged", "llmoe_unpack",
+           "llmoe_dispatch_unpack",
            "llmoe_signal_workspace_bytes", "llmoe_dispatch_signaled", "llmoe_dispatch_signaled_static", "llmoe_clean",
            "llmoe_get_error",
            "llmoe_status_string")
@@ -95,6 +96,8 @@ _lib.llmoe_combine_staged.argtypes = [_P, _P, _P, _P, _BS, _P]
 _lib.llmoe_combine_staged.restype = _I
 _lib.llmoe_unpack.argtypes = [_P, _P, _BS, _P]
 _lib.llmoe_unpack.restype = _I
+_lib.llmoe_dispatch_unpack.argtypes = [_P, _P, _P, _P, _BS, _P]
+_lib.llmoe_dispatch_unpack.restype = _I
 _lib.llmoe_signal_workspace_bytes.argtypes = [_BS]
 _lib.llmoe_signal_workspace_bytes.restype = ctypes.c_size_t
 _lib.llmoe_dispatch_signaled.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int64, _BS, _P]
@@ -205,6 +208,12 @@ def llmoe_combine_staged(y, topk_idx, topk_w, out, bs: llmoe_buf_set_t, stream=N
 def llmoe_unpack(recv_x, recv_src, bs: llmoe_buf_set_t, stream=None) -> None:
     _check(_lib.llmoe_unpack(_addr(recv_x, "payload"), _addr(recv_src, "i32"), ctypes.byref(bs), _stream(stream)),
            "llmoe_unpack")
+
+
+def llmoe_dispatch_unpack(x, topk_idx, recv_x, recv_src, bs: llmoe_buf_set_t, stream=None) -> None:
+    _check(_lib.llmoe_dispatch_unpack(_addr(x, "payload"), _addr(topk_idx, "i64"), _addr(recv_x, "payload"),
+                                      _addr(recv_src, "i32"), ctypes.byref(bs), _stream(stream)),
+           "llmoe_dispatch_unpack")
 
 
 def llmoe_signal_workspace_bytes(bs: llmoe_buf_set_t) -> int:

@@ -8,10 +8,11 @@ known, small number of times, on a workload small enough that a capture of
 all its sections ends quickly (dense16: 2.35 GB on the device).
 
     python -m combine_routing_count_prefix_gb300.profile_calls --workload dense16 \\
-        --calls route,clean,dispatch,combine,unpack,signaled,staged --reps 3
+        --calls route,clean,dispatch,combine,unpack,signaled,staged,dispatch_unpack --reps 3
 
 Kernels per call: route -> route_kernel; clean -> clean_kernel; dispatch ->
-dispatch_kernel; combine -> combine_kernel<payload type>; unpack ->
+dispatch_kernel<false>; dispatch_unpack -> dispatch_kernel<true> (the dispatch
+that also writes the experts' input rows); combine -> combine_kernel<payload type>; unpack ->
 unpack_balanced_kernel (fewer buckets than routed entries) or unpack_kernel
 (otherwise, e.g. many_small); signaled -> dispatch_signaled_kernel; staged ->
 combine_put_kernel, then combine_reduce_ring_kernel (more (token, chunk) units
@@ -37,7 +38,7 @@ FLUSH_READ_BYTES = 256 << 20
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--workload", default="dense16")
-    ap.add_argument("--calls", default="route,clean,dispatch,combine,unpack,signaled,staged")
+    ap.add_argument("--calls", default="route,clean,dispatch,combine,unpack,signaled,staged,dispatch_unpack")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args(argv)
 
@@ -68,7 +69,7 @@ def main(argv=None):
     rows = w.E * w.R * w.T
     recv_x = recv_src = ws = slot = counts = None
     calls = args.calls.split(",")
-    if "unpack" in calls or "signaled" in calls:
+    if "unpack" in calls or "signaled" in calls or "dispatch_unpack" in calls:
         recv_x = torch.empty((rows, w.H), dtype=torch.int16, device="cuda")
         recv_src = torch.empty((rows,), dtype=torch.int32, device="cuda")
         ws = torch.zeros(llmoe.llmoe_signal_workspace_bytes(bs0) // 4, dtype=torch.int32, device="cuda")
@@ -100,6 +101,10 @@ def main(argv=None):
                 dispatched()
                 flush()
                 llmoe.llmoe_unpack(recv_x, recv_src, bs0)
+            elif name == "dispatch_unpack":
+                llmoe.llmoe_clean(bs0)
+                flush()
+                llmoe.llmoe_dispatch_unpack(x, idx, recv_x, recv_src, bs0)
             elif name == "signaled":
                 llmoe.llmoe_clean(bs0)
                 flush()

@@ -237,6 +237,18 @@ LLMOE_API int llmoe_combine_staged(const void* y, const int64_t* topk_idx, const
  * Uses no routing input: the counts in the rank buffers drive it. */
 LLMOE_API int llmoe_unpack(void* recv_x, int32_t* recv_src, const llmoe_buf_set_t* bs, llmoe_stream_t stream);
 
+/* Dispatch with the experts' input rows: the messages and recv-count words of
+ * llmoe_dispatch, and in the same launch the recv_x rows and recv_src words
+ * that llmoe_unpack would make from them (same layout and rows; rows past a
+ * bucket's count are not written).  The CTA that moves a token holds its row
+ * and knows its slots, so it writes each row straight to recv_x beside the
+ * message, and no message is read back.  The result equals llmoe_dispatch
+ * followed by llmoe_unpack.  recv_x and recv_src as for llmoe_unpack (16- and
+ * 4-byte aligned, not NULL); they must not overlap the rank buffers, x or
+ * topk_idx.  Flags as for llmoe_dispatch. */
+LLMOE_API int llmoe_dispatch_unpack(const void* x, const int64_t* topk_idx, void* recv_x, int32_t* recv_src,
+                                    const llmoe_buf_set_t* bs, llmoe_stream_t stream);
+
 /* Bytes of the workspace llmoe_dispatch_signaled needs for this geometry.
  * No counterpart in the layout header: it holds one completion counter per
  * source rank (producers) and one for the consumers. */

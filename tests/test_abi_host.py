@@ -94,6 +94,7 @@ def test_invalid_buf_set_rejected_before_launch(lib, kw):
         lambda: lib._lib.llmoe_dispatch(A, A, ctypes.byref(bs), None),
         lambda: lib._lib.llmoe_combine(A, A, A, 2 * A, ctypes.byref(bs), None),
         lambda: lib._lib.llmoe_clean(ctypes.byref(bs), None),
+        lambda: lib._lib.llmoe_dispatch_unpack(A, A, 2 * A, 3 * A, ctypes.byref(bs), None),
     ]
     for c in calls:
         assert c() == lib.LLMOE_ERR_INVALID_ARGUMENT
@@ -112,6 +113,12 @@ def test_invalid_pointers_rejected_before_launch(lib):
     assert L.llmoe_combine(A, A, A, A + 4096, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT
     assert L.llmoe_route(A, A, None, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT
     assert L.llmoe_dispatch(A, A, None, None) == lib.LLMOE_ERR_INVALID_ARGUMENT
+    # the dispatch with the experts' rows: recv_x / recv_src missing or misaligned
+    assert L.llmoe_dispatch_unpack(A, A, None, 3 * A, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT
+    assert L.llmoe_dispatch_unpack(A, A, 2 * A, None, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT
+    assert L.llmoe_dispatch_unpack(A, A, 2 * A + 8, 3 * A, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT
+    assert L.llmoe_dispatch_unpack(A, A, 2 * A, 3 * A + 2, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT
+    assert L.llmoe_dispatch_unpack(None, A, 2 * A, 3 * A, ctypes.byref(bs), None) == lib.LLMOE_ERR_INVALID_ARGUMENT
     code = ctypes.c_int32()
     assert L.llmoe_get_error(ctypes.byref(bs), None, ctypes.byref(code), 0) == lib.LLMOE_ERR_INVALID_USAGE
 

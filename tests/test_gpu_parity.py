@@ -708,6 +708,57 @@ def test_unpack_shapes(L, R, E, K, H, T, dtype):
     assert r.error() == 0
     r.check_dispatch()
     check_unpack(r, recv_x2, recv_src2)
+    recv_x3, recv_src3 = unpack_buffers(w, dtype)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch_unpack(r.x, r.idx, recv_x3, recv_src3, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    r.check_dispatch()
+    check_unpack(r, recv_x3, recv_src3)
+
+
+# the dispatch that writes the experts' input rows itself: messages, counts
+# and rows equal llmoe_dispatch followed by llmoe_unpack (oracle), nothing
+# else in the rank buffers written; repeated on the same buffers
+@pytest.mark.parametrize("name,dtype", [("tiny", "bf16"), ("dsv3", "bf16"), ("skewed", "bf16"), ("many_small", "bf16"),
+                                        ("skewed", "fp32"), ("many_small", "fp16"), ("dense16", "bf16")])
+def test_dispatch_unpack(L, name, dtype):
+    w = WORKLOADS[name]
+    r = Round(L, w, seed=87, dtype=dtype)
+    recv_x, recv_src = unpack_buffers(w, dtype)
+    for rep in range(2):
+        L.llmoe_clean(r.bs_d)
+        L.llmoe_dispatch_unpack(r.x, r.idx, recv_x, recv_src, r.bs_d)
+        torch.cuda.synchronize()
+        assert r.error() == 0
+        d = r.check_dispatch()
+        check_unpack(r, recv_x, recv_src)
+    r.check_canary(d)
+
+
+@pytest.mark.parametrize("name,tokens,dispatch_set", [("dsv3", 1, 1), ("dsv3", 37, 0), ("skewed", 0, 1),
+                                                      ("many_small", 9, 0), ("large", 599, 1)])
+def test_dispatch_unpack_fewer_tokens_flags_and_set(L, name, tokens, dispatch_set):
+    # a ragged call on either set, with both flags; then the identity-expert
+    # layer over its rows
+    w = WORKLOADS[name]
+    r = Round(L, w, seed=88, tokens=tokens, dispatch_set=dispatch_set)
+    recv_x, recv_src = unpack_buffers(w)
+    F = L.LLMOE_FLAG_CLEAN_OTHER_SET | L.LLMOE_FLAG_INPUTS_READY
+    bs = r.rb.buf_set(r.ds, w.K, r.T_call, r.err, flags=F)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch_unpack(r.x, r.idx, recv_x, recv_src, bs)
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    assert not r.rb.signal_words(r.cs).any(), "the other set was cleaned"
+    r.check_dispatch()
+    check_unpack(r, recv_x, recv_src)
+    if tokens:
+        L.llmoe_combine(recv_x, r.idx, r.wt, r.out, r.bs_c)
+        torch.cuda.synchronize()
+        u = oracle.unpack(r.inp["x"], r.inp["topk_idx"], w.E, num_max_tokens=w.T)
+        ref, _ = oracle.combine(u["recv_x"], r.inp["topk_idx"], r.inp["topk_w"], w.H, w.E, num_max_tokens=w.T)
+        assert np.array_equal(r.out.cpu().numpy().view(np.uint16), ref)
 
 
 @pytest.mark.parametrize("name,dtype", [("tiny", "bf16"), ("dsv3", "bf16"), ("skewed", "bf16"), ("many_small", "fp16")])
