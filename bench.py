@@ -902,6 +902,25 @@ def copy_ceiling(hin, hout, reps: int = 20) -> dict:
         us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
         nbytes = src.numel() * src.element_size()
         res[name] = {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1), "bytes": nbytes}
+    # both directions at once, each on its own stream, as the e2e steps run them
+    s_up, s_down = torch.cuda.Stream(), torch.cuda.Stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(cur)
+    for s in (s_up, s_down):
+        s.wait_event(a)
+    for _ in range(reps):
+        with torch.cuda.stream(s_up):
+            din.copy_(hin, non_blocking=True)
+        with torch.cuda.stream(s_down):
+            hout.copy_(dout, non_blocking=True)
+    for s in (s_up, s_down):
+        cur.wait_stream(s)
+    b.record(cur)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / reps
+    nbytes = hin.numel() * hin.element_size() + dout.numel() * dout.element_size()
+    res["both"] = {"us": round(us, 2), "gbs": round(nbytes / us / 1e3, 1), "bytes": nbytes,
+                   "note": "one upload and one download at once per pair, on two streams"}
     return res
 
 
