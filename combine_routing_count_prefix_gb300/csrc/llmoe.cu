@@ -15,20 +15,23 @@
 //     histogram of the tokens before the CTA's block (integer atomics: the
 //     result does not depend on their order) plus an in-block rank; no
 //     global atomics and no scratch memory.
-//   dispatch_kernel: one producer lane streams the CTA's x rows into a
+//   dispatch_kernel<kRows>: one producer lane streams the CTA's x rows into a
 //     shared-memory ring (cp.async.bulk, mbarrier); each consumer thread owns a
 //     16-byte quad of a chunk and writes it to the token's K messages.  A
 //     message is 4 + H * sizeof(T) bytes, 4 (mod 16) when H * sizeof(T) is a
 //     multiple of 16, so a destination starts at any 4-byte phase: the quad is
 //     shifted by whole 32-bit words and stored aligned, with 4/8-byte stores
-//     only at a message's head and tail.
+//     only at a message's head and tail.  With kRows the quad also goes, as it
+//     is, to the entry's row of the experts' input (llmoe_dispatch_unpack).
 //   combine_kernel<T>: each warp reduces 32 quads of one output row: up to 8
 //     aligned 16-byte loads of expert rows, fp32 products rounded then added
 //     in ascending k (__fmul_rn / __fadd_rn: never contracted to an FMA), the
 //     sum stored as T (bf16 / fp16 rounded to nearest even).
-//   combine_put_kernel, combine_reduce_kernel<T>: the staged combine through
-//     the combine receive buffers (messages written with realigned stores,
-//     read at their own 4-byte alignment).
+//   combine_put_kernel, combine_reduce_ring_kernel<T> / combine_reduce_kernel<T>:
+//     the staged combine through the combine receive buffers (messages written
+//     with realigned stores; read back through a shared-memory ring of bulk
+//     copies for large grids, or at their own 4-byte alignment into registers
+//     for small ones).
 //   unpack_balanced_kernel, unpack_kernel: received messages to the experts'
 //     input layout, driven by the count words.
 //   dispatch_signaled_kernel: dispatch and unpack in one cooperative launch;
