@@ -736,6 +736,57 @@ def test_dispatch_unpack(L, name, dtype):
     r.check_canary(d)
 
 
+@pytest.mark.parametrize("bad", [8, 1 << 40, -2])
+def test_dispatch_unpack_bad_expert_reported_and_skipped(L, bad):
+    # an id outside [-1, E): reported in validate mode, and neither a message
+    # nor a row is written for it
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, seed=1)
+    inp["topk_idx"][1, 3, 1] = bad
+    r = Round(L, w, inp=inp)
+    recv_x, recv_src = unpack_buffers(w)
+    L.llmoe_clean(r.bs_d)
+    L.llmoe_dispatch_unpack(r.x, r.idx, recv_x, recv_src, r.bs_d)
+    torch.cuda.synchronize()
+    assert r.error() == L.LLMOE_DEV_BAD_EXPERT
+    masked = inp["topk_idx"].copy()
+    masked[1, 3, 1] = -1
+    d = oracle.dispatch(inp["x"], masked, w.E, num_max_tokens=w.T)
+    r.check_dispatch(d)
+    r.inp = dict(inp, topk_idx=masked)
+    check_unpack(r, recv_x, recv_src)
+    r.check_canary(d)
+
+
+def test_dispatch_unpack_in_cuda_graph(L):
+    # captured once, replayed on canary-filled buffers
+    w = WORKLOADS["skewed"]
+    r = Round(L, w, seed=89)
+    recv_x, recv_src = unpack_buffers(w)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        L.llmoe_clean(r.bs_d)
+        L.llmoe_dispatch_unpack(r.x, r.idx, recv_x, recv_src, r.bs_d)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        L.llmoe_clean(r.bs_d)
+        L.llmoe_dispatch_unpack(r.x, r.idx, recv_x, recv_src, r.bs_d)
+    r.rb.storage.fill_(CANARY)
+    recv_x2, recv_src2 = unpack_buffers(w)
+    recv_x.copy_(recv_x2)
+    recv_src.copy_(recv_src2)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert r.error() == 0
+    d = r.check_dispatch()
+    check_unpack(r, recv_x, recv_src)
+    r.check_canary(d)
+
+
 @pytest.mark.parametrize("name,tokens,dispatch_set", [("dsv3", 1, 1), ("dsv3", 37, 0), ("skewed", 0, 1),
                                                       ("many_small", 9, 0), ("large", 599, 1)])
 def test_dispatch_unpack_fewer_tokens_flags_and_set(L, name, tokens, dispatch_set):
