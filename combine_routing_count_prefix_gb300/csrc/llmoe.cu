@@ -829,6 +829,14 @@ __device__ __forceinline__ uint4 shfl_idx16(const uint4& v, int src_lane) {
 #define LLMOE_UNPACK_MIN_BLOCKS 4
 #endif
 constexpr int kRowBatch = LLMOE_ROW_BATCH;
+// The staged put's token blocks are sized for two waves of CTAs, not one:
+// with one token per CTA and 1.7 waves instead of two tokens per CTA and one
+// wave, the CTA scheduler gives the SMs that move rows fastest more of them
+// (staged combine 73.0 -> 71.5 us on DS-V3, Large 503 -> 500 us).  The ring
+// reduce stays at one wave: two took DS-V3 to 75.5 and skewed to 37.0 us.
+#ifndef LLMOE_PUT_WAVES
+#define LLMOE_PUT_WAVES 2
+#endif
 #ifndef LLMOE_PUT_BATCH
 #define LLMOE_PUT_BATCH 4
 #endif
@@ -2190,7 +2198,7 @@ int llmoe_combine_staged(const void* y, const int64_t* topk_idx, const float* to
     if (ob < ye && yb < oe) return LLMOE_ERR_INVALID_ARGUMENT;
   }
   const size_t put_extra = (sizeof(void*) + sizeof(uintptr_t)) * (size_t)g.K;
-  set_blocking(&g, blocks_per_sm(kslot(kCombinePutKernel), (const void*)combine_put_kernel, kThreads,
+  set_blocking(&g, LLMOE_PUT_WAVES * blocks_per_sm(kslot(kCombinePutKernel), (const void*)combine_put_kernel, kThreads,
                                  route_smem_bytes(g) + put_extra));
   const size_t smem = route_smem_bytes(g) + (sizeof(void*) + sizeof(uintptr_t)) * (size_t)g.TB * g.K;
   if ((rc = set_smem(kslot(kCombinePutKernel), (const void*)combine_put_kernel, smem)) != LLMOE_SUCCESS) return rc;
