@@ -936,9 +936,9 @@ def run_e2e_pipelined(args, llmoe, w, hins, houts, rb, tokens, stream):
     kernel's launch behind its predecessor's drain (programmatic dependent
     launch) with the cleans fused into the data kernels.  Kernels of
     consecutive steps on two streams, each step on its own buffer set, took
-    108 us a layer against 103-105 this way: the cleans that schedule needs,
-    and launches no longer hidden behind a predecessor, cost more than the
-    overlap gained."""
+    108 us a layer against 103-105 with this schedule (both with dispatch
+    then unpack): the cleans that schedule needs, and launches no longer
+    hidden behind a predecessor, cost more than the overlap gained."""
     import torch
 
     hin, hout = hins[0], houts[0]
